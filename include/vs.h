@@ -1,0 +1,233 @@
+/*
+ * vs.h -- C ABI of libvs: sparse x dense products over CSR and the
+ * value-grouped VCS layout, on one GB300 GPU (sm_103a).
+ *
+ * What the library computes (page title, section):
+ *
+ *  - "Add CUDA transfer and matmul kernels for the normalized views"
+ *    (vsparse PR #61), "The layout stays compressed": a VCS matrix keeps, for
+ *    each major slice, its nonzeros grouped into runs that share one value:
+ *    major_ptr -> (values, value_ptr) -> indices.  It is never expanded to one
+ *    float per nonzero.  VCSR: major = rows; VCSC: major = columns.
+ *  - Same page, "The kernels": four product directions, VCSR@B, VCSC@B, B@VCSR
+ *    and B@VCSC.  A direction is "aligned" when the output's disjoint axis is
+ *    the major one (VCSR@B, B@VCSC) and "misaligned" otherwise.
+ *  - "Regridder" (regridding PR #70), "How it is built": CSR assembly is a
+ *    counting sort (count each row's entries, then place them at the rows'
+ *    cursors); a row keeps its entries in element order.  Products are
+ *    row-parallel with a thread group whose size depends only on the matrix,
+ *    so a product repeats exactly and a column gives the same numbers alone
+ *    or in a batch.  The exact transpose is kept once built.
+ *
+ * Conventions shared by every entry point:
+ *
+ *  - All device pointers are caller-owned unless stated otherwise.  A handle
+ *    owns copies of the matrix arrays and any scratch it needs; it keeps no
+ *    pointer to caller memory after its build call returns.
+ *  - Every call is enqueued on the caller's `stream` and is asynchronous,
+ *    except where a call documents a synchronisation.  The caller keeps the
+ *    buffers alive until the stream has passed the call.
+ *  - Errors are returned as vs_status; nothing is thrown across the ABI.
+ *    vs_last_error() gives a message for the calling thread's last failure.
+ *    On error, output buffers are left in an unspecified state.
+ *  - Index arrays are int32; nnz must be below 2^31.
+ *  - Dense operands are described by vs_dense (logical rows x cols plus
+ *    strides in elements).  The width axis of B and out must have stride 1:
+ *    for A@B that is the column axis (row-major B and out); for B@A it is the
+ *    row axis (B and out stored column-major).  Otherwise VS_ERR_LAYOUT.
+ *  - out is overwritten (beta = 0).  A slice with no entries yields zeros.
+ *    B and out must not overlap.
+ */
+#ifndef VS_H
+#define VS_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct vs_handle_s *vs_handle;
+
+typedef enum {
+    VS_OK = 0,
+    VS_ERR_INVALID = 1,     /* bad argument, unknown enum value, NULL handle/pointer */
+    VS_ERR_SHAPE = 2,       /* operand shapes do not match the matrix and direction */
+    VS_ERR_LAYOUT = 3,      /* width axis not contiguous, or overlapping operands */
+    VS_ERR_RANGE = 4,       /* a COO coordinate lies outside the matrix */
+    VS_ERR_ALLOC = 5,       /* device or host allocation failed */
+    VS_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+    VS_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up */
+    VS_ERR_UNSUPPORTED = 8, /* valid request this build does not implement */
+    VS_ERR_NAN = 9          /* a NaN value where VCS needs a run key */
+} vs_status;
+
+typedef enum { VS_F32 = 0, VS_F64 = 1 } vs_dtype;
+typedef enum { VS_MAJOR_ROW = 0, VS_MAJOR_COL = 1 } vs_major;
+typedef enum { VS_A_B = 0, VS_B_A = 1 } vs_direction;
+typedef enum { VS_LAYOUT_CSR = 0, VS_LAYOUT_VCS = 1 } vs_layout;
+
+/*
+ * Product variants.  Aligned directions always run the deterministic gather;
+ * the variant matters only for misaligned directions (VCSC@B, B@VCSR, CSC@B,
+ * B@CSR):
+ *   VS_DETERMINISTIC  two-phase scheme: per-block partial sums in shared
+ *                     memory over tiles of the output, then a combine in a
+ *                     fixed chunk order.  Bit-identical on repeats.
+ *   VS_ATOMIC         zero-fill out, then scatter with atomic adds (the pages'
+ *                     design); not bit-reproducible.
+ *   VS_TRANSPOSED     the aligned gather over the exact transpose held by the
+ *                     handle (see vs_attach_transpose); bit-identical on repeats.
+ */
+typedef enum { VS_DETERMINISTIC = 0, VS_ATOMIC = 1, VS_TRANSPOSED = 2 } vs_variant;
+
+typedef struct {
+    void *ptr;            /* first element */
+    int64_t rows, cols;   /* logical shape */
+    int64_t row_stride;   /* elements between (r, c) and (r+1, c) */
+    int64_t col_stride;   /* elements between (r, c) and (r, c+1) */
+    vs_dtype dtype;
+} vs_dense;
+
+typedef struct {
+    int32_t layout;         /* vs_layout */
+    int32_t major;          /* vs_major */
+    int32_t dtype;          /* vs_dtype of the stored values */
+    int32_t group_size;     /* g: threads that share one slice, a power of two in [1, 32] */
+    int64_t n_rows, n_cols; /* matrix shape */
+    int64_t nnz;            /* stored entries (explicit zeros and duplicates kept) */
+    int64_t n_runs;         /* VCS: number of runs R; CSR: nnz */
+    int64_t chunk_len;      /* L: slices longer than L are split into chunks of L entries */
+    int64_t n_long_slices;  /* slices longer than L */
+    int64_t n_chunks;       /* chunks over all long slices */
+    int32_t has_transpose;  /* 1 once vs_attach_transpose succeeded */
+    int32_t reserved;
+} vs_info_t;
+
+typedef struct {
+    const int32_t *ptr;       /* n_major+1: CSR slice starts, or VCS major_ptr (run starts) */
+    const int32_t *indices;   /* nnz minor indices */
+    const void *values;       /* CSR: nnz values of the handle dtype; VCS: R float32 run values */
+    const int32_t *value_ptr; /* VCS: R+1 index starts of the runs; CSR: NULL */
+    int64_t n_major, nnz, n_runs;
+} vs_arrays;
+
+/*
+ * vs_build_csr -- CSR (major = VS_MAJOR_ROW) or CSC (VS_MAJOR_COL) of COO
+ * triples by a stable counting sort on the device ("Regridder", "How it is
+ * built"): per-slice counts, exclusive scan into the slice pointer, then
+ * placement at slice cursors so that every slice keeps its entries in COO
+ * input order.  Duplicates and explicit zeros are kept; values are copied
+ * bit for bit.
+ *
+ *   n_rows, n_cols   matrix shape (>= 0, < 2^31)
+ *   nnz              number of triples (>= 0, < 2^31)
+ *   d_row, d_col     device int32[nnz] coordinates
+ *   d_val            device values[nnz] of `dtype` (float32 or float64)
+ *   major            VS_MAJOR_ROW for CSR, VS_MAJOR_COL for CSC
+ *   stream           stream the build runs on
+ *   out              receives the new handle (owned by the caller; vs_destroy)
+ *
+ * Synchronises `stream` once, to read back the coordinate-range check.
+ * Returns VS_ERR_RANGE if a coordinate lies outside the matrix.
+ */
+vs_status vs_build_csr(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
+                       const int32_t *d_col, const void *d_val, vs_dtype dtype, vs_major major,
+                       cudaStream_t stream, vs_handle *out);
+
+/*
+ * vs_build_vcs -- VCSR (major = VS_MAJOR_ROW) or VCSC (VS_MAJOR_COL) of COO
+ * triples ("Add CUDA transfer and matmul kernels ...", "The layout stays
+ * compressed").  Entries are stably sorted on the device by the key
+ * (major, value, minor), the value ordered by the IEEE total order of its
+ * float32 bits (-0.0 and +0.0 form separate runs).  A run is a maximal group
+ * with equal (major, value); runs of a slice are in ascending value, indices
+ * in a run ascending.  Values are float32 (all device floating-point arrays of
+ * the view are float32 on that page).
+ *
+ * Arguments as for vs_build_csr, with float32 values.  Synchronises `stream`
+ * once to read back the run count and checks.  Returns VS_ERR_NAN for a NaN
+ * value, VS_ERR_RANGE for an out-of-range coordinate.
+ */
+vs_status vs_build_vcs(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
+                       const int32_t *d_col, const float *d_val, vs_major major,
+                       cudaStream_t stream, vs_handle *out);
+
+/*
+ * vs_spmm -- out = A @ B (dir = VS_A_B) or out = B @ A (dir = VS_B_A).
+ *
+ *   A        handle from vs_build_csr / vs_build_vcs
+ *   B        device operand: A@B: n_cols x w, column stride 1;
+ *                            B@A: w x n_rows, row stride 1
+ *   out      device output:  A@B: n_rows x w, column stride 1;
+ *                            B@A: w x n_cols, row stride 1
+ *   dir      VS_A_B or VS_B_A
+ *   variant  see vs_variant (matters for misaligned directions only)
+ *   stream   stream the product runs on
+ *
+ * B and out have the handle's dtype; vector loads are used when the width and
+ * strides are multiples of 16 bytes and the pointers are 16-byte aligned.
+ * w = 0 or an empty matrix returns VS_OK after writing zeros where out has
+ * elements.  No allocation happens here for VS_ATOMIC and for aligned
+ * directions; VS_DETERMINISTIC on a misaligned direction may grow the
+ * handle's scratch on first use with a new width (stream-ordered).  Calls on
+ * the same handle must not overlap on the GPU (they share scratch).
+ * VS_TRANSPOSED needs vs_attach_transpose first, else VS_ERR_INVALID.
+ */
+vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direction dir,
+                  vs_variant variant, cudaStream_t stream);
+
+/*
+ * vs_spmm_host -- vs_spmm with B and out in HOST memory (pinned memory is
+ * fastest).  Copies B to device staging owned by the handle, runs vs_spmm on
+ * `stream`, copies the result back and synchronises `stream` before
+ * returning, so `out` is ready on return.  Layout rules as for vs_spmm.  The
+ * staging buffers grow on first use with a larger operand.
+ */
+vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_host,
+                       vs_direction dir, vs_variant variant, cudaStream_t stream);
+
+/*
+ * vs_attach_transpose -- builds the exact transpose of A from A's own arrays
+ * and keeps it in the handle ("Regridder", "API": the exact transpose, kept
+ * once built).  For VCSR that is the VCSC of the same matrix (and vice versa);
+ * for CSR it is the CSC whose slices list entries in CSR order.  Afterwards
+ * VS_TRANSPOSED runs misaligned directions as aligned gathers over it.
+ * Synchronises `stream` once.  Idempotent.
+ */
+vs_status vs_attach_transpose(vs_handle A, cudaStream_t stream);
+
+/* vs_info -- shape, layout and matrix-only kernel parameters of A. */
+vs_status vs_info(vs_handle A, vs_info_t *info);
+
+/* vs_export -- read-only device pointers to A's layout arrays (owned by A,
+ * valid until vs_destroy). */
+vs_status vs_export(vs_handle A, vs_arrays *arrays);
+
+/*
+ * vs_handle_bytes -- device bytes held by A: `layout_bytes` counts the layout
+ * arrays only (for VCS: major_ptr, values, value_ptr, indices -- no per-nonzero
+ * value array exists), `scratch_bytes` counts everything else (chunk tables,
+ * partial-sum scratch, staging, an attached transpose).  Either may be NULL.
+ */
+vs_status vs_handle_bytes(vs_handle A, int64_t *layout_bytes, int64_t *scratch_bytes);
+
+/* vs_destroy -- frees everything A owns.  Synchronises the device first, so
+ * work still queued on A finishes before its memory is released.  NULL is OK. */
+vs_status vs_destroy(vs_handle A);
+
+/* Static text for a status code. */
+const char *vs_status_string(vs_status s);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char *vs_last_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t vs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VS_H */

@@ -1,0 +1,676 @@
+// assembly.cu -- device construction of CSR/CSC and VCSR/VCSC from COO.
+//
+// "Regridder" (regridding PR #70), "How it is built": assembly is a counting
+// sort.  One pass counts each slice's entries, an exclusive scan turns the
+// counts into slice starts, and a placement pass puts every entry at its
+// slice's cursor so that a slice keeps its entries in input order.
+//
+// The placement must be stable and bit-identical on every run, so it is done
+// as an LSD radix sort of a permutation with 8-bit digits: each pass counts
+// digits per tile of 2048 entries, scans the (digit, tile) counts, and scatters
+// with ranks that follow input order inside a tile (warp match + per-warp
+// digit counters, then a prefix over warps).  Every count is an integer, so
+// the result does not depend on scheduling.  No kernel waits on another
+// block: scans are reduce-then-scan with separate launches.
+//
+// VCS ("Add CUDA transfer and matmul kernels for the normalized views", "The
+// layout stays compressed") sorts by the key (major, value, minor), LSD order:
+// minor first, then the value's total-order bits, then major.  Passes whose
+// bits never vary, or whose order the input already has, are skipped.
+#include <algorithm>
+#include <vector>
+
+#include "device_utils.cuh"
+#include "vs_internal.h"
+
+namespace vs {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kItems = 8;
+constexpr int kTile = kThreads * kItems;  // 2048 entries per tile
+
+// ------------------------------------------------------------------ temporaries
+
+// Stream-ordered temporary device memory, released when it goes out of scope.
+struct Temp {
+  void *p = nullptr;
+  cudaStream_t s;
+  explicit Temp(cudaStream_t st) : s(st) {}
+  vs_status alloc(size_t bytes) {
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMallocAsync(&p, bytes, s);
+    if (e != cudaSuccess) {
+      p = nullptr;
+      return cuda_status(e, "cudaMallocAsync (assembly temporary)");
+    }
+    return VS_OK;
+  }
+  ~Temp() {
+    if (p) cudaFreeAsync(p, s);
+  }
+  template <typename T>
+  T *as() const {
+    return static_cast<T *>(p);
+  }
+};
+
+vs_status dev_alloc(void **p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    return e == cudaErrorMemoryAllocation ? (set_error("device allocation failed"), VS_ERR_ALLOC)
+                                          : cuda_status(e, "cudaMalloc");
+  }
+  return VS_OK;
+}
+
+inline unsigned grid_for(int64_t n, int per_block) {
+  return (unsigned)std::max<int64_t>(1, (n + per_block - 1) / per_block);
+}
+
+inline int bit_length(uint64_t x) {
+  int b = 0;
+  while (x) {
+    ++b;
+    x >>= 1;
+  }
+  return b;
+}
+
+// ------------------------------------------------------------------ scan
+
+// sums[b] = sum of in[b*kTile .. (b+1)*kTile)
+__global__ void scan_reduce_kernel(const int32_t *__restrict__ in, int64_t n,
+                                   int32_t *__restrict__ sums) {
+  const int64_t base = (int64_t)blockIdx.x * kTile;
+  int local = 0;
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    int64_t i = base + k * kThreads + threadIdx.x;
+    if (i < n) local += in[i];
+  }
+  int total;
+  block_exclusive_scan<kThreads>(local, total);
+  if (threadIdx.x == 0) sums[blockIdx.x] = total;
+}
+
+// out[i] = offsets[b] + exclusive prefix of in inside tile b; out[n] = grand total.
+__global__ void scan_apply_kernel(const int32_t *__restrict__ in, int64_t n,
+                                  const int32_t *__restrict__ offsets, int32_t *__restrict__ out) {
+  const int64_t base = (int64_t)blockIdx.x * kTile + (int64_t)threadIdx.x * kItems;
+  int v[kItems];
+  int local = 0;
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    int64_t i = base + k;
+    v[k] = i < n ? in[i] : 0;
+    local += v[k];
+  }
+  int total;
+  int run = block_exclusive_scan<kThreads>(local, total) + (offsets ? offsets[blockIdx.x] : 0);
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    int64_t i = base + k;
+    if (i < n) out[i] = run;
+    run += v[k];
+  }
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == kThreads - 1) out[n] = run;
+}
+
+// Exclusive scan of in[0..n) into out[0..n], out[n] = total.  Integer-exact.
+vs_status exclusive_scan(const int32_t *in, int32_t *out, int64_t n, cudaStream_t s) {
+  const int64_t nb = (n + kTile - 1) / kTile;
+  if (nb <= 1) {
+    scan_apply_kernel<<<1, kThreads, 0, s>>>(in, n, nullptr, out);
+    VS_CUDA(cudaGetLastError());
+    return VS_OK;
+  }
+  Temp sums(s), offs(s);
+  VS_TRY(sums.alloc(sizeof(int32_t) * nb));
+  VS_TRY(offs.alloc(sizeof(int32_t) * (nb + 1)));
+  scan_reduce_kernel<<<(unsigned)nb, kThreads, 0, s>>>(in, n, sums.as<int32_t>());
+  VS_CUDA(cudaGetLastError());
+  VS_TRY(exclusive_scan(sums.as<int32_t>(), offs.as<int32_t>(), nb, s));
+  scan_apply_kernel<<<(unsigned)nb, kThreads, 0, s>>>(in, n, offs.as<int32_t>(), out);
+  VS_CUDA(cudaGetLastError());
+  return VS_OK;
+}
+
+// ------------------------------------------------------------------ radix sort of a permutation
+
+__device__ __forceinline__ int digit_of(const int32_t *perm, const uint32_t *key, int64_t i,
+                                        int shift) {
+  int64_t e = perm ? perm[i] : i;
+  return (int)((key[e] >> shift) & 0xFFu);
+}
+
+__global__ void radix_hist_kernel(const int32_t *__restrict__ perm, const uint32_t *__restrict__ key,
+                                  int64_t n, int shift, int32_t *__restrict__ hist, int64_t ntiles) {
+  __shared__ int h[256];
+  h[threadIdx.x] = 0;
+  __syncthreads();
+  const int64_t base = (int64_t)blockIdx.x * kTile;
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    int64_t i = base + k * kThreads + threadIdx.x;
+    if (i < n) atomicAdd(&h[digit_of(perm, key, i, shift)], 1);
+  }
+  __syncthreads();
+  hist[(int64_t)threadIdx.x * ntiles + blockIdx.x] = h[threadIdx.x];
+}
+
+// Stable scatter: inside a tile, warp w owns entries [w*256, (w+1)*256) and
+// walks them 32 at a time in order; equal digits are ranked by lane order.
+__global__ void radix_scatter_kernel(const int32_t *__restrict__ perm_in,
+                                     const uint32_t *__restrict__ key, int64_t n, int shift,
+                                     const int32_t *__restrict__ offsets, int64_t ntiles,
+                                     int32_t *__restrict__ perm_out) {
+  __shared__ int wcount[kThreads / 32][256];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int d = threadIdx.x; d < (kThreads / 32) * 256; d += kThreads) (&wcount[0][0])[d] = 0;
+  __syncthreads();
+  int dig[kItems], rank[kItems], elem[kItems];
+  const int64_t wbase = (int64_t)blockIdx.x * kTile + (int64_t)w * (kItems * 32);
+  const unsigned lt = lanemask_lt();
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    const int64_t i = wbase + it * 32 + lane;
+    const bool valid = i < n;
+    const int e = valid ? (perm_in ? perm_in[i] : (int)i) : -1;
+    const int d = valid ? (int)((key[e] >> shift) & 0xFFu) : 256;
+    const unsigned peers = __match_any_sync(kFullMask, d);
+    const int before = __popc(peers & lt);
+    const int base = valid ? wcount[w][d] : 0;
+    __syncwarp();
+    if (valid && before == 0) wcount[w][d] = base + __popc(peers);
+    __syncwarp();
+    dig[it] = d;
+    rank[it] = base + before;
+    elem[it] = e;
+  }
+  __syncthreads();
+  {  // exclusive prefix over warps, per digit (thread = digit)
+    const int d = threadIdx.x;
+    int run = 0;
+#pragma unroll
+    for (int ww = 0; ww < kThreads / 32; ++ww) {
+      int c = wcount[ww][d];
+      wcount[ww][d] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    if (dig[it] < 256) {
+      const int64_t pos =
+          (int64_t)offsets[(int64_t)dig[it] * ntiles + blockIdx.x] + wcount[w][dig[it]] + rank[it];
+      perm_out[pos] = elem[it];
+    }
+  }
+}
+
+// Sorts the permutation *perm (nullptr = identity) stably by key bits
+// [bit_lo, bit_hi) in 8-bit digits.  buf0/buf1 are int32[n] ping-pong buffers;
+// on return *perm points at the one holding the result.
+vs_status radix_passes(const int32_t **perm, const uint32_t *key, int64_t n, int bit_lo,
+                       int bit_hi, int32_t *buf0, int32_t *buf1, cudaStream_t s) {
+  if (bit_hi <= bit_lo || n <= 1) return VS_OK;
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  Temp hist(s), offs(s);
+  VS_TRY(hist.alloc(sizeof(int32_t) * 256 * ntiles));
+  VS_TRY(offs.alloc(sizeof(int32_t) * (256 * ntiles + 1)));
+  for (int shift = bit_lo; shift < bit_hi; shift += 8) {
+    int32_t *dst = (*perm == buf0) ? buf1 : buf0;
+    radix_hist_kernel<<<(unsigned)ntiles, kThreads, 0, s>>>(*perm, key, n, shift,
+                                                            hist.as<int32_t>(), ntiles);
+    VS_CUDA(cudaGetLastError());
+    VS_TRY(exclusive_scan(hist.as<int32_t>(), offs.as<int32_t>(), 256 * ntiles, s));
+    radix_scatter_kernel<<<(unsigned)ntiles, kThreads, 0, s>>>(*perm, key, n, shift,
+                                                               offs.as<int32_t>(), ntiles, dst);
+    VS_CUDA(cudaGetLastError());
+    *perm = dst;
+  }
+  return VS_OK;
+}
+
+// ------------------------------------------------------------------ checks and keys
+
+struct Checks {
+  int range_error;     // a coordinate outside the matrix
+  int nan_error;       // a NaN value (VCS only)
+  int major_unsorted;  // major[t] < major[t-1] somewhere
+  int minor_unsorted;  // minor[t] < minor[t-1] somewhere
+  int lex_unsorted;    // (major, minor)[t] < (major, minor)[t-1] somewhere
+  unsigned key_or;     // OR of the value keys
+  unsigned key_and;    // AND of the value keys
+  int pad;
+};
+
+// Total-order key of a float32: negative values flip every bit, others set the sign bit.
+__device__ __forceinline__ uint32_t order_key(uint32_t b) {
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__global__ void check_kernel(const int32_t *__restrict__ maj, const int32_t *__restrict__ mnr,
+                             const float *__restrict__ val, int64_t nnz, int64_t n_major,
+                             int64_t n_minor, uint32_t *__restrict__ vkey, Checks *out) {
+  int range = 0, nan = 0, mu = 0, nu = 0, lu = 0;
+  unsigned kor = 0, kand = 0xffffffffu;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < nnz;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int a = maj[t], b = mnr[t];
+    if (a < 0 || a >= n_major || b < 0 || b >= n_minor) range = 1;
+    if (t > 0) {
+      const int pa = maj[t - 1], pb = mnr[t - 1];
+      if (a < pa) mu = 1;
+      if (b < pb) nu = 1;
+      if (a < pa || (a == pa && b < pb)) lu = 1;
+    }
+    if (val) {
+      const uint32_t bits = __float_as_uint(val[t]);
+      if ((bits & 0x7fffffffu) > 0x7f800000u) nan = 1;
+      const uint32_t k = order_key(bits);
+      vkey[t] = k;
+      kor |= k;
+      kand &= k;
+    }
+  }
+  range = __syncthreads_or(range);
+  nan = __syncthreads_or(nan);
+  mu = __syncthreads_or(mu);
+  nu = __syncthreads_or(nu);
+  lu = __syncthreads_or(lu);
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) {
+    kor |= __shfl_xor_sync(kFullMask, kor, d);
+    kand &= __shfl_xor_sync(kFullMask, kand, d);
+  }
+  if (threadIdx.x == 0) {
+    if (range) atomicOr(&out->range_error, 1);
+    if (nan) atomicOr(&out->nan_error, 1);
+    if (mu) atomicOr(&out->major_unsorted, 1);
+    if (nu) atomicOr(&out->minor_unsorted, 1);
+    if (lu) atomicOr(&out->lex_unsorted, 1);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicOr(&out->key_or, kor);
+    atomicAnd(&out->key_and, kand);
+  }
+}
+
+__global__ void copy_key_kernel(const int32_t *__restrict__ src, uint32_t *__restrict__ dst,
+                                int64_t n) {
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n;
+       t += (int64_t)gridDim.x * blockDim.x)
+    dst[t] = (uint32_t)src[t];
+}
+
+__global__ void count_kernel(const int32_t *__restrict__ maj, int64_t n, int32_t *__restrict__ cnt) {
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n;
+       t += (int64_t)gridDim.x * blockDim.x)
+    atomicAdd(&cnt[maj[t]], 1);
+}
+
+// dst_idx[i] = mnr[perm[i]]; dst_val[i] = val[perm[i]] (raw `words` 32-bit words each).
+__global__ void gather_entries_kernel(const int32_t *__restrict__ perm,
+                                      const int32_t *__restrict__ mnr,
+                                      const uint32_t *__restrict__ val, int words, int64_t n,
+                                      int32_t *__restrict__ dst_idx, uint32_t *__restrict__ dst_val) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = perm ? perm[i] : i;
+    dst_idx[i] = mnr[e];
+    if (dst_val)
+      for (int k = 0; k < words; ++k) dst_val[i * words + k] = val[e * words + k];
+  }
+}
+
+// Run starts of the sorted VCS entries: flag[i] = 1 where (major, value) changes.
+__global__ void run_flag_kernel(const int32_t *__restrict__ perm, const int32_t *__restrict__ maj,
+                                const uint32_t *__restrict__ vkey, int64_t n,
+                                int32_t *__restrict__ flag) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = perm ? perm[i] : i;
+    int f = 1;
+    if (i > 0) {
+      const int64_t p = perm ? perm[i - 1] : i - 1;
+      f = (maj[e] != maj[p]) || (vkey[e] != vkey[p]);
+    }
+    flag[i] = f;
+  }
+}
+
+__global__ void run_fill_kernel(const int32_t *__restrict__ perm, const int32_t *__restrict__ maj,
+                                const float *__restrict__ val, const int32_t *__restrict__ flag,
+                                const int32_t *__restrict__ run_id, int64_t n,
+                                int32_t *__restrict__ vptr, float *__restrict__ values,
+                                int32_t *__restrict__ runs_per_major) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (!flag[i]) continue;
+    const int64_t e = perm ? perm[i] : i;
+    const int r = run_id[i];
+    vptr[r] = (int32_t)i;
+    values[r] = val[e];
+    atomicAdd(&runs_per_major[maj[e]], 1);
+  }
+}
+
+__global__ void set_int_kernel(int32_t *p, int32_t v) { *p = v; }
+
+constexpr unsigned kGridCap = 152 * 16;
+
+}  // namespace
+
+// ------------------------------------------------------------------ build_matrix
+
+vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dtype, int64_t n_rows,
+                       int64_t n_cols, int64_t nnz, const int32_t *d_row, const int32_t *d_col,
+                       const void *d_val, cudaStream_t s) {
+  m.layout = layout;
+  m.major = major;
+  m.dtype = dtype;
+  m.n_rows = n_rows;
+  m.n_cols = n_cols;
+  m.n_major = major == VS_MAJOR_ROW ? n_rows : n_cols;
+  m.n_minor = major == VS_MAJOR_ROW ? n_cols : n_rows;
+  m.nnz = nnz;
+  const int32_t *maj = major == VS_MAJOR_ROW ? d_row : d_col;
+  const int32_t *mnr = major == VS_MAJOR_ROW ? d_col : d_row;
+  const bool vcs = layout == VS_LAYOUT_VCS;
+  const size_t dsize = m.dsize();
+
+  // ---- checks (and value keys for VCS)
+  Temp checks(s), vkey(s);
+  VS_TRY(checks.alloc(sizeof(Checks)));
+  Checks init{};
+  init.key_and = 0xffffffffu;
+  VS_CUDA(cudaMemcpyAsync(checks.p, &init, sizeof init, cudaMemcpyHostToDevice, s));
+  if (vcs) VS_TRY(vkey.alloc(sizeof(uint32_t) * (size_t)std::max<int64_t>(nnz, 1)));
+  if (nnz > 0) {
+    check_kernel<<<std::min<unsigned>(kGridCap, grid_for(nnz, 256)), 256, 0, s>>>(
+        maj, mnr, vcs ? static_cast<const float *>(d_val) : nullptr, nnz, m.n_major, m.n_minor,
+        vkey.as<uint32_t>(), checks.as<Checks>());
+    VS_CUDA(cudaGetLastError());
+  }
+  Checks ck{};
+  VS_CUDA(cudaMemcpyAsync(&ck, checks.p, sizeof ck, cudaMemcpyDeviceToHost, s));
+  VS_CUDA(cudaStreamSynchronize(s));
+  if (ck.range_error) {
+    set_error("a COO coordinate lies outside the matrix");
+    return VS_ERR_RANGE;
+  }
+  if (ck.nan_error) {
+    set_error("NaN value: VCS runs need an ordered value key");
+    return VS_ERR_NAN;
+  }
+
+  // ---- the permutation that orders the entries
+  Temp b0(s), b1(s), keybuf(s);
+  VS_TRY(b0.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(nnz, 1)));
+  VS_TRY(b1.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(nnz, 1)));
+  VS_TRY(keybuf.alloc(sizeof(uint32_t) * (size_t)std::max<int64_t>(nnz, 1)));
+  const int32_t *perm = nullptr;  // identity
+  const unsigned eg = std::min<unsigned>(kGridCap, grid_for(nnz, 256));
+  if (vcs) {
+    // minor first (unless the input already orders it), then value bits, then major
+    if (ck.minor_unsorted && ck.lex_unsorted && nnz > 1) {
+      copy_key_kernel<<<eg, 256, 0, s>>>(mnr, keybuf.as<uint32_t>(), nnz);
+      VS_CUDA(cudaGetLastError());
+      VS_TRY(radix_passes(&perm, keybuf.as<uint32_t>(), nnz, 0,
+                          bit_length((uint64_t)std::max<int64_t>(m.n_minor - 1, 0)),
+                          b0.as<int32_t>(), b1.as<int32_t>(), s));
+    }
+    const unsigned diff = ck.key_or ^ ck.key_and;
+    if (diff && nnz > 1) {
+      const int lo = __builtin_ctz(diff), hi = 32 - __builtin_clz(diff);
+      VS_TRY(radix_passes(&perm, vkey.as<uint32_t>(), nnz, lo, hi, b0.as<int32_t>(),
+                          b1.as<int32_t>(), s));
+    }
+    if (nnz > 1 && (ck.major_unsorted || diff || (ck.minor_unsorted && ck.lex_unsorted))) {
+      copy_key_kernel<<<eg, 256, 0, s>>>(maj, keybuf.as<uint32_t>(), nnz);
+      VS_CUDA(cudaGetLastError());
+      VS_TRY(radix_passes(&perm, keybuf.as<uint32_t>(), nnz, 0,
+                          bit_length((uint64_t)std::max<int64_t>(m.n_major - 1, 0)),
+                          b0.as<int32_t>(), b1.as<int32_t>(), s));
+    }
+  } else if (ck.major_unsorted && nnz > 1) {
+    copy_key_kernel<<<eg, 256, 0, s>>>(maj, keybuf.as<uint32_t>(), nnz);
+    VS_CUDA(cudaGetLastError());
+    VS_TRY(radix_passes(&perm, keybuf.as<uint32_t>(), nnz, 0,
+                        bit_length((uint64_t)std::max<int64_t>(m.n_major - 1, 0)),
+                        b0.as<int32_t>(), b1.as<int32_t>(), s));
+  }
+
+  // ---- owned arrays: slice pointer and indices (padded for vector over-reads)
+  VS_TRY(dev_alloc((void **)&m.ptr, sizeof(int32_t) * (m.n_major + 1)));
+  VS_TRY(dev_alloc((void **)&m.idx, sizeof(int32_t) * (nnz + 16)));
+  VS_CUDA(cudaMemsetAsync(m.idx, 0, sizeof(int32_t) * (nnz + 16), s));
+  Temp cnt(s);
+  VS_TRY(cnt.alloc(sizeof(int32_t) * (m.n_major + 1)));
+  VS_CUDA(cudaMemsetAsync(cnt.p, 0, sizeof(int32_t) * (m.n_major + 1), s));
+
+  if (!vcs) {
+    VS_TRY(dev_alloc(&m.vals, dsize * (nnz + 16)));
+    VS_CUDA(cudaMemsetAsync(m.vals, 0, dsize * (nnz + 16), s));
+    if (nnz > 0) {
+      gather_entries_kernel<<<eg, 256, 0, s>>>(perm, mnr, static_cast<const uint32_t *>(d_val),
+                                               (int)(dsize / 4), nnz, m.idx,
+                                               static_cast<uint32_t *>(m.vals));
+      VS_CUDA(cudaGetLastError());
+      count_kernel<<<eg, 256, 0, s>>>(maj, nnz, cnt.as<int32_t>());
+      VS_CUDA(cudaGetLastError());
+    }
+    VS_TRY(exclusive_scan(cnt.as<int32_t>(), m.ptr, m.n_major, s));
+    m.R = nnz;
+    VS_CUDA(cudaStreamSynchronize(s));
+    return VS_OK;
+  }
+
+  // ---- VCS: runs
+  Temp flag(s), run_id(s);
+  VS_TRY(flag.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(nnz, 1)));
+  VS_TRY(run_id.alloc(sizeof(int32_t) * (nnz + 1)));
+  int32_t R = 0;
+  if (nnz > 0) {
+    gather_entries_kernel<<<eg, 256, 0, s>>>(perm, mnr, nullptr, 0, nnz, m.idx, nullptr);
+    VS_CUDA(cudaGetLastError());
+    run_flag_kernel<<<eg, 256, 0, s>>>(perm, maj, vkey.as<uint32_t>(), nnz, flag.as<int32_t>());
+    VS_CUDA(cudaGetLastError());
+    VS_TRY(exclusive_scan(flag.as<int32_t>(), run_id.as<int32_t>(), nnz, s));
+    VS_CUDA(cudaMemcpyAsync(&R, run_id.as<int32_t>() + nnz, sizeof R, cudaMemcpyDeviceToHost, s));
+    VS_CUDA(cudaStreamSynchronize(s));
+  }
+  m.R = R;
+  VS_TRY(dev_alloc(&m.vals, sizeof(float) * (R + 16)));
+  VS_TRY(dev_alloc((void **)&m.vptr, sizeof(int32_t) * (R + 16)));
+  VS_CUDA(cudaMemsetAsync(m.vals, 0, sizeof(float) * (R + 16), s));
+  VS_CUDA(cudaMemsetAsync(m.vptr, 0, sizeof(int32_t) * (R + 16), s));
+  if (nnz > 0) {
+    run_fill_kernel<<<eg, 256, 0, s>>>(perm, maj, static_cast<const float *>(d_val),
+                                       flag.as<int32_t>(), run_id.as<int32_t>(), nnz, m.vptr,
+                                       static_cast<float *>(m.vals), cnt.as<int32_t>());
+    VS_CUDA(cudaGetLastError());
+  }
+  set_int_kernel<<<1, 1, 0, s>>>(m.vptr + R, (int32_t)nnz);
+  VS_CUDA(cudaGetLastError());
+  VS_TRY(exclusive_scan(cnt.as<int32_t>(), m.ptr, m.n_major, s));
+  VS_CUDA(cudaStreamSynchronize(s));
+  return VS_OK;
+}
+
+// ------------------------------------------------------------------ transpose
+
+namespace {
+
+// COO of a stored layout, in layout order: (major, minor, value bits).
+__global__ void expand_csr_kernel(const int32_t *__restrict__ ptr, int64_t n_major,
+                                  int32_t *__restrict__ out_major) {
+  for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < n_major;
+       s += (int64_t)gridDim.x * blockDim.x)
+    for (int32_t k = ptr[s]; k < ptr[s + 1]; ++k) out_major[k] = (int32_t)s;
+}
+
+__global__ void expand_vcs_kernel(const int32_t *__restrict__ major_ptr,
+                                  const int32_t *__restrict__ vptr, const float *__restrict__ values,
+                                  int64_t n_major, int32_t *__restrict__ out_major,
+                                  float *__restrict__ out_val) {
+  for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < n_major;
+       s += (int64_t)gridDim.x * blockDim.x)
+    for (int32_t r = major_ptr[s]; r < major_ptr[s + 1]; ++r)
+      for (int32_t k = vptr[r]; k < vptr[r + 1]; ++k) {
+        out_major[k] = (int32_t)s;
+        out_val[k] = values[r];
+      }
+}
+
+}  // namespace
+
+vs_status build_transpose(const Matrix &src, Matrix &dst, cudaStream_t s) {
+  const int64_t nnz = src.nnz;
+  Temp maj(s), vals(s);
+  VS_TRY(maj.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(nnz, 1)));
+  const unsigned g = std::min<unsigned>(kGridCap, grid_for(src.n_major, 256));
+  const void *val_ptr = src.vals;
+  if (src.layout == VS_LAYOUT_CSR) {
+    if (src.n_major > 0) {
+      expand_csr_kernel<<<g, 256, 0, s>>>(src.ptr, src.n_major, maj.as<int32_t>());
+      VS_CUDA(cudaGetLastError());
+    }
+  } else {
+    VS_TRY(vals.alloc(sizeof(float) * (size_t)std::max<int64_t>(nnz, 1)));
+    if (src.n_major > 0) {
+      expand_vcs_kernel<<<g, 256, 0, s>>>(src.ptr, src.vptr, static_cast<const float *>(src.vals),
+                                          src.n_major, maj.as<int32_t>(), vals.as<float>());
+      VS_CUDA(cudaGetLastError());
+    }
+    val_ptr = vals.p;
+  }
+  // the stored major axis becomes the minor axis of the transpose
+  const vs_major other = src.major == VS_MAJOR_ROW ? VS_MAJOR_COL : VS_MAJOR_ROW;
+  const int32_t *rows = src.major == VS_MAJOR_ROW ? maj.as<int32_t>() : src.idx;
+  const int32_t *cols = src.major == VS_MAJOR_ROW ? src.idx : maj.as<int32_t>();
+  return build_matrix(dst, src.layout, other, src.dtype, src.n_rows, src.n_cols, nnz, rows, cols,
+                      val_ptr, s);
+}
+
+// ------------------------------------------------------------------ matrix-only parameters
+
+namespace {
+__global__ void mark_starts_kernel(const int32_t *__restrict__ seg_ptr, int64_t n_seg,
+                                   uint8_t *__restrict__ start) {
+  for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < n_seg;
+       s += (int64_t)gridDim.x * blockDim.x)
+    start[seg_ptr[s]] = 1;
+}
+__global__ void unsorted_kernel(const int32_t *__restrict__ idx, const uint8_t *__restrict__ start,
+                                int64_t n, int *flag) {
+  int bad = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x + 1; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    if (!start[i] && idx[i] < idx[i - 1]) bad = 1;
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
+}
+}  // namespace
+
+vs_status prepare_matrix(Matrix &m, cudaStream_t s) {
+  // slice entry ranges on the host
+  std::vector<int32_t> ptr(m.n_major + 1), vptr;
+  VS_CUDA(cudaMemcpyAsync(ptr.data(), m.ptr, sizeof(int32_t) * (m.n_major + 1),
+                          cudaMemcpyDeviceToHost, s));
+  if (m.layout == VS_LAYOUT_VCS) {
+    vptr.resize(m.R + 1);
+    VS_CUDA(cudaMemcpyAsync(vptr.data(), m.vptr, sizeof(int32_t) * (m.R + 1),
+                            cudaMemcpyDeviceToHost, s));
+  }
+  // are the minor indices ascending inside every segment (row or run)?
+  int unsorted = 0;
+  if (m.layout == VS_LAYOUT_VCS) {
+    m.sorted_segments = true;  // by construction
+  } else if (m.nnz > 1) {
+    Temp start(s), flag(s);
+    VS_TRY(start.alloc(m.nnz + 1));
+    VS_TRY(flag.alloc(sizeof(int)));
+    VS_CUDA(cudaMemsetAsync(start.p, 0, m.nnz + 1, s));
+    VS_CUDA(cudaMemsetAsync(flag.p, 0, sizeof(int), s));
+    mark_starts_kernel<<<std::min<unsigned>(kGridCap, grid_for(m.n_major, 256)), 256, 0, s>>>(
+        m.ptr, m.n_major, start.as<uint8_t>());
+    VS_CUDA(cudaGetLastError());
+    unsorted_kernel<<<std::min<unsigned>(kGridCap, grid_for(m.nnz, 256)), 256, 0, s>>>(
+        m.idx, start.as<uint8_t>(), m.nnz, flag.as<int>());
+    VS_CUDA(cudaGetLastError());
+    VS_CUDA(cudaMemcpyAsync(&unsorted, flag.p, sizeof(int), cudaMemcpyDeviceToHost, s));
+    VS_CUDA(cudaStreamSynchronize(s));
+    m.sorted_segments = !unsorted;
+  } else {
+    m.sorted_segments = true;
+  }
+  VS_CUDA(cudaStreamSynchronize(s));
+  auto entry = [&](int64_t sl) -> int64_t {
+    return m.layout == VS_LAYOUT_VCS ? vptr[ptr[sl]] : ptr[sl];
+  };
+
+  // group size g: the largest power of two <= the mean entries per slice, in [1, 32]
+  int g = 1;
+  if (m.n_major > 0) {
+    const int64_t mean = m.nnz / m.n_major;
+    while (g * 2 <= mean && g < 32) g *= 2;
+  }
+  m.g = g;
+  m.L = kChunkLen;
+
+  // chunk tasks of the long slices
+  std::vector<int4> tasks;
+  int64_t n_long = 0;
+  for (int64_t sl = 0; sl < m.n_major; ++sl) {
+    const int64_t len = entry(sl + 1) - entry(sl);
+    if (len <= m.L) continue;
+    const int64_t nch = (len + m.L - 1) / m.L;
+    const int64_t first = (int64_t)tasks.size();
+    for (int64_t k = 0; k < nch; ++k)
+      tasks.push_back(make_int4((int)sl, (int)k, (int)n_long, (int)first));
+    ++n_long;
+  }
+  m.n_long = n_long;
+  m.n_chunks = (int64_t)tasks.size();
+  if (m.n_chunks > 0) {
+    VS_TRY(dev_alloc((void **)&m.chunk_tasks, sizeof(int4) * m.n_chunks));
+    VS_CUDA(cudaMemcpyAsync(m.chunk_tasks, tasks.data(), sizeof(int4) * m.n_chunks,
+                            cudaMemcpyHostToDevice, s));
+    VS_TRY(dev_alloc((void **)&m.counters, sizeof(int) * n_long));
+    VS_CUDA(cudaMemsetAsync(m.counters, 0, sizeof(int) * n_long, s));
+    VS_TRY(dev_alloc(&m.partials, m.dsize() * kMaxBlockWidth * m.n_chunks));
+  }
+
+  // two-phase chunking: C contiguous slice ranges with balanced entry counts.
+  // C depends on the matrix only; it is kept small when the scattered output
+  // is large, so that C partial copies of it stay bounded (64 MiB at width 64).
+  {
+    int64_t c_nnz = std::max<int64_t>(1, (m.nnz + 32767) / 32768);
+    const int64_t out_row_bytes = (int64_t)m.dsize() * kMaxBlockWidth;
+    int64_t c_mem = std::max<int64_t>(1, (int64_t(1) << 26) / std::max<int64_t>(1, m.n_minor * out_row_bytes));
+    int64_t C = std::min<int64_t>(std::min(c_nnz, c_mem), 256);
+    C = std::max<int64_t>(1, std::min<int64_t>(C, std::max<int64_t>(m.n_major, 1)));
+    std::vector<int32_t> bounds(C + 1);
+    bounds[0] = 0;
+    int64_t sl = 0;
+    for (int64_t c = 1; c < C; ++c) {
+      const int64_t target = m.nnz * c / C;
+      while (sl < m.n_major && entry(sl) < target) ++sl;
+      bounds[c] = (int32_t)sl;
+    }
+    bounds[C] = (int32_t)m.n_major;
+    m.tp_chunks = (int)C;
+    VS_TRY(dev_alloc((void **)&m.tp_bounds, sizeof(int32_t) * (C + 1)));
+    VS_CUDA(cudaMemcpyAsync(m.tp_bounds, bounds.data(), sizeof(int32_t) * (C + 1),
+                            cudaMemcpyHostToDevice, s));
+  }
+  VS_CUDA(cudaStreamSynchronize(s));
+  return VS_OK;
+}
+
+}  // namespace vs

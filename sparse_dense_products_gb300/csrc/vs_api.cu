@@ -1,0 +1,364 @@
+// vs_api.cu -- the C ABI of libvs: argument checking, handle lifetime and the
+// mapping of the six products onto the two kernel families.
+//
+// Transpose identity: VCSC(A) holds exactly the arrays of VCSR(A^T), and a
+// width-contiguous B@A is (A^T B^T) in row-major terms.  So every product is
+// one of two kernels in a "slice frame" -- slices are the stored major axis,
+// entries carry the minor index t:
+//   aligned    (A@B with major = rows, B@A with major = columns):
+//              Y[slice] = sum a * X[t]          (gather.cu)
+//   misaligned (A@B with major = columns, B@A with major = rows):
+//              Y[t]    += a * X[slice]          (scatter.cu)
+// ("Add CUDA transfer and matmul kernels for the normalized views", "The
+// kernels": the same two binary choices as the host kernels.)
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "vs_internal.h"
+
+namespace vs {
+
+namespace {
+thread_local std::string g_last_error;
+}
+
+void set_error(const std::string &msg) { g_last_error = msg; }
+const char *last_error() { return g_last_error.c_str(); }
+
+vs_status cuda_status(cudaError_t e, const char *what) {
+  set_error(std::string(what) + ": " + cudaGetErrorString(e));
+  if (e == cudaErrorMemoryAllocation) return VS_ERR_ALLOC;
+  return VS_ERR_CUDA;
+}
+
+int64_t Matrix::layout_bytes() const {
+  int64_t b = (int64_t)sizeof(int32_t) * (n_major + 1) + (int64_t)sizeof(int32_t) * nnz;
+  if (layout == VS_LAYOUT_VCS)
+    b += (int64_t)sizeof(float) * R + (int64_t)sizeof(int32_t) * (R + 1);
+  else
+    b += (int64_t)dsize() * nnz;
+  return b;
+}
+
+int64_t Matrix::meta_bytes() const {
+  return (int64_t)sizeof(int4) * n_chunks + (int64_t)sizeof(int) * n_long +
+         (int64_t)dsize() * kMaxBlockWidth * n_chunks + (int64_t)sizeof(int32_t) * (tp_chunks + 1);
+}
+
+void free_matrix(Matrix &m) {
+  for (void *p : {(void *)m.ptr, (void *)m.idx, m.vals, (void *)m.vptr, (void *)m.chunk_tasks,
+                  (void *)m.counters, m.partials, (void *)m.tp_bounds})
+    if (p) cudaFree(p);
+  m.ptr = m.idx = m.vptr = m.tp_bounds = nullptr;
+  m.vals = m.partials = nullptr;
+  m.chunk_tasks = nullptr;
+  m.counters = nullptr;
+}
+
+vs_status Scratch::reserve(size_t need, cudaStream_t s) {
+  if (need <= bytes) return VS_OK;
+  if (p) cudaFreeAsync(p, s);
+  p = nullptr;
+  bytes = 0;
+  cudaError_t e = cudaMallocAsync(&p, need, s);
+  if (e != cudaSuccess) {
+    p = nullptr;
+    return cuda_status(e, "cudaMallocAsync (handle scratch)");
+  }
+  bytes = need;
+  return VS_OK;
+}
+
+void Scratch::release() {
+  if (p) cudaFree(p);
+  p = nullptr;
+  bytes = 0;
+}
+
+}  // namespace vs
+
+using namespace vs;
+
+namespace {
+
+vs_status invalid(const char *msg) {
+  set_error(msg);
+  return VS_ERR_INVALID;
+}
+
+bool valid_handle(vs_handle h) { return h != nullptr; }
+
+vs_status build_common(vs_layout layout, int64_t n_rows, int64_t n_cols, int64_t nnz,
+                       const int32_t *d_row, const int32_t *d_col, const void *d_val,
+                       vs_dtype dtype, vs_major major, cudaStream_t stream, vs_handle *out) {
+  if (!out) return invalid("out handle pointer is NULL");
+  *out = nullptr;
+  if (n_rows < 0 || n_cols < 0 || nnz < 0) return invalid("negative size");
+  if (n_rows >= (int64_t(1) << 31) || n_cols >= (int64_t(1) << 31) || nnz >= (int64_t(1) << 31)) {
+    set_error("sizes must be below 2^31 (int32 indices)");
+    return VS_ERR_UNSUPPORTED;
+  }
+  if (dtype != VS_F32 && dtype != VS_F64) return invalid("unknown dtype");
+  if (major != VS_MAJOR_ROW && major != VS_MAJOR_COL) return invalid("unknown major");
+  if (nnz > 0 && (!d_row || !d_col || !d_val)) return invalid("NULL COO pointer");
+  vs_handle h = new (std::nothrow) vs_handle_s();
+  if (!h) {
+    set_error("host allocation failed");
+    return VS_ERR_ALLOC;
+  }
+  cudaGetDevice(&h->device);
+  vs_status st = build_matrix(h->A, layout, major, dtype, n_rows, n_cols, nnz, d_row, d_col, d_val,
+                              stream);
+  if (st == VS_OK) st = prepare_matrix(h->A, stream);
+  if (st != VS_OK) {
+    std::string msg = last_error();
+    cudaStreamSynchronize(stream);
+    free_matrix(h->A);
+    delete h;
+    set_error(msg);
+    return st;
+  }
+  *out = h;
+  return VS_OK;
+}
+
+int64_t extent_bytes(const vs_dense &d) {
+  if (d.rows <= 0 || d.cols <= 0) return 0;
+  const int64_t es = d.dtype == VS_F64 ? 8 : 4;
+  return ((d.rows - 1) * d.row_stride + (d.cols - 1) * d.col_stride + 1) * es;
+}
+
+// Maps (A, B, out, dir) onto the slice frame.  Fills X, Y and w.
+vs_status frame(const Matrix &m, const vs_dense &B, const vs_dense &out, vs_direction dir,
+                DenseView &X, DenseView &Y, int64_t &w, bool &aligned) {
+  if (dir != VS_A_B && dir != VS_B_A) return invalid("unknown direction");
+  if (B.dtype != m.dtype || out.dtype != m.dtype) {
+    set_error("B and out must have the matrix dtype (VCS: float32)");
+    return VS_ERR_INVALID;
+  }
+  if (B.rows < 0 || B.cols < 0 || out.rows < 0 || out.cols < 0) return invalid("negative shape");
+  if (dir == VS_A_B) {
+    w = B.cols;
+    if (B.rows != m.n_cols || out.rows != m.n_rows || out.cols != w) {
+      set_error("A@B needs B: n_cols x w and out: n_rows x w");
+      return VS_ERR_SHAPE;
+    }
+    if (w > 1 && (B.col_stride != 1 || out.col_stride != 1)) {
+      set_error("A@B needs column stride 1 for B and out (row-major)");
+      return VS_ERR_LAYOUT;
+    }
+    if ((B.rows > 1 && B.row_stride < w) || (out.rows > 1 && out.row_stride < w)) {
+      set_error("row stride smaller than the width");
+      return VS_ERR_LAYOUT;
+    }
+    X = DenseView{B.ptr, B.rows, B.rows > 1 ? B.row_stride : w};
+    Y = DenseView{out.ptr, out.rows, out.rows > 1 ? out.row_stride : w};
+  } else {
+    w = B.rows;
+    if (B.cols != m.n_rows || out.cols != m.n_cols || out.rows != w) {
+      set_error("B@A needs B: w x n_rows and out: w x n_cols");
+      return VS_ERR_SHAPE;
+    }
+    if (w > 1 && (B.row_stride != 1 || out.row_stride != 1)) {
+      set_error("B@A needs row stride 1 for B and out (column-major)");
+      return VS_ERR_LAYOUT;
+    }
+    if ((B.cols > 1 && B.col_stride < w) || (out.cols > 1 && out.col_stride < w)) {
+      set_error("column stride smaller than the width");
+      return VS_ERR_LAYOUT;
+    }
+    X = DenseView{B.ptr, B.cols, B.cols > 1 ? B.col_stride : w};
+    Y = DenseView{out.ptr, out.cols, out.cols > 1 ? out.col_stride : w};
+  }
+  if (w > 0 && Y.rows > 0 && !Y.p) return invalid("out pointer is NULL");
+  if (w > 0 && X.rows > 0 && !X.p) return invalid("B pointer is NULL");
+  // B and out must not overlap
+  const int64_t bx = extent_bytes(B), ox = extent_bytes(out);
+  if (bx > 0 && ox > 0) {
+    const char *b0 = static_cast<const char *>(B.ptr), *o0 = static_cast<const char *>(out.ptr);
+    if (b0 < o0 + ox && o0 < b0 + bx) {
+      set_error("B and out overlap");
+      return VS_ERR_LAYOUT;
+    }
+  }
+  aligned = (dir == VS_A_B) == (m.major == VS_MAJOR_ROW);
+  return VS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vs_status vs_build_csr(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
+                       const int32_t *d_col, const void *d_val, vs_dtype dtype, vs_major major,
+                       cudaStream_t stream, vs_handle *out) {
+  return build_common(VS_LAYOUT_CSR, n_rows, n_cols, nnz, d_row, d_col, d_val, dtype, major,
+                      stream, out);
+}
+
+vs_status vs_build_vcs(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
+                       const int32_t *d_col, const float *d_val, vs_major major,
+                       cudaStream_t stream, vs_handle *out) {
+  return build_common(VS_LAYOUT_VCS, n_rows, n_cols, nnz, d_row, d_col, d_val, VS_F32, major,
+                      stream, out);
+}
+
+vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direction dir,
+                  vs_variant variant, cudaStream_t stream) {
+  if (!valid_handle(A)) return invalid("NULL handle");
+  if (!B || !out) return invalid("NULL operand descriptor");
+  if (variant != VS_DETERMINISTIC && variant != VS_ATOMIC && variant != VS_TRANSPOSED)
+    return invalid("unknown variant");
+  DenseView X, Y;
+  int64_t w = 0;
+  bool aligned = false;
+  VS_TRY(frame(A->A, *B, *out, dir, X, Y, w, aligned));
+  if (w == 0 || Y.rows == 0) return VS_OK;
+  if (aligned) return launch_gather(A->A, X, Y, w, stream);
+  switch (variant) {
+    case VS_ATOMIC:
+      return launch_scatter_atomic(A->A, X, Y, w, stream);
+    case VS_TRANSPOSED:
+      if (!A->T) return invalid("VS_TRANSPOSED needs vs_attach_transpose first");
+      return launch_gather(*A->T, X, Y, w, stream);
+    default:
+      return launch_scatter_two_phase(*A, A->A, X, Y, w, stream);
+  }
+}
+
+vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_host,
+                       vs_direction dir, vs_variant variant, cudaStream_t stream) {
+  if (!valid_handle(A)) return invalid("NULL handle");
+  if (!B_host || !out_host) return invalid("NULL operand descriptor");
+  DenseView X, Y;
+  int64_t w = 0;
+  bool aligned = false;
+  VS_TRY(frame(A->A, *B_host, *out_host, dir, X, Y, w, aligned));
+  if (w == 0 || Y.rows == 0) return VS_OK;
+  const size_t es = A->A.dsize();
+  const int64_t wpad = (w + 3) / 4 * 4;  // keep device rows 16-byte aligned
+  VS_TRY(A->stage_B.reserve((size_t)std::max<int64_t>(X.rows, 1) * wpad * es, stream));
+  VS_TRY(A->stage_out.reserve((size_t)Y.rows * wpad * es, stream));
+  if (X.rows > 0)
+    VS_CUDA(cudaMemcpy2DAsync(A->stage_B.p, wpad * es, X.p, X.ld * es, w * es, X.rows,
+                              cudaMemcpyHostToDevice, stream));
+  vs_dense Bd{}, Od{};
+  if (dir == VS_A_B) {
+    Bd = vs_dense{A->stage_B.p, B_host->rows, B_host->cols, wpad, 1, B_host->dtype};
+    Od = vs_dense{A->stage_out.p, out_host->rows, out_host->cols, wpad, 1, out_host->dtype};
+  } else {
+    Bd = vs_dense{A->stage_B.p, B_host->rows, B_host->cols, 1, wpad, B_host->dtype};
+    Od = vs_dense{A->stage_out.p, out_host->rows, out_host->cols, 1, wpad, out_host->dtype};
+  }
+  VS_TRY(vs_spmm(A, &Bd, &Od, dir, variant, stream));
+  VS_CUDA(cudaMemcpy2DAsync(Y.p, Y.ld * es, A->stage_out.p, wpad * es, w * es, Y.rows,
+                            cudaMemcpyDeviceToHost, stream));
+  VS_CUDA(cudaStreamSynchronize(stream));
+  return VS_OK;
+}
+
+vs_status vs_attach_transpose(vs_handle A, cudaStream_t stream) {
+  if (!valid_handle(A)) return invalid("NULL handle");
+  if (A->T) return VS_OK;
+  Matrix *t = new (std::nothrow) Matrix();
+  if (!t) {
+    set_error("host allocation failed");
+    return VS_ERR_ALLOC;
+  }
+  vs_status st = build_transpose(A->A, *t, stream);
+  if (st == VS_OK) st = prepare_matrix(*t, stream);
+  if (st != VS_OK) {
+    std::string msg = last_error();
+    cudaStreamSynchronize(stream);
+    free_matrix(*t);
+    delete t;
+    set_error(msg);
+    return st;
+  }
+  A->T = t;
+  return VS_OK;
+}
+
+vs_status vs_info(vs_handle A, vs_info_t *info) {
+  if (!valid_handle(A) || !info) return invalid("NULL argument");
+  const Matrix &m = A->A;
+  std::memset(info, 0, sizeof *info);
+  info->layout = m.layout;
+  info->major = m.major;
+  info->dtype = m.dtype;
+  info->group_size = m.g;
+  info->n_rows = m.n_rows;
+  info->n_cols = m.n_cols;
+  info->nnz = m.nnz;
+  info->n_runs = m.R;
+  info->chunk_len = m.L;
+  info->n_long_slices = m.n_long;
+  info->n_chunks = m.n_chunks;
+  info->has_transpose = A->T != nullptr;
+  return VS_OK;
+}
+
+vs_status vs_export(vs_handle A, vs_arrays *arrays) {
+  if (!valid_handle(A) || !arrays) return invalid("NULL argument");
+  const Matrix &m = A->A;
+  arrays->ptr = m.ptr;
+  arrays->indices = m.idx;
+  arrays->values = m.vals;
+  arrays->value_ptr = m.layout == VS_LAYOUT_VCS ? m.vptr : nullptr;
+  arrays->n_major = m.n_major;
+  arrays->nnz = m.nnz;
+  arrays->n_runs = m.R;
+  return VS_OK;
+}
+
+vs_status vs_handle_bytes(vs_handle A, int64_t *layout_bytes, int64_t *scratch_bytes) {
+  if (!valid_handle(A)) return invalid("NULL handle");
+  if (layout_bytes) *layout_bytes = A->A.layout_bytes();
+  if (scratch_bytes) {
+    int64_t s = A->A.meta_bytes() + (int64_t)A->tp_partials.bytes + (int64_t)A->tp_table.bytes +
+                (int64_t)A->stage_B.bytes + (int64_t)A->stage_out.bytes;
+    if (A->T) s += A->T->layout_bytes() + A->T->meta_bytes();
+    *scratch_bytes = s;
+  }
+  return VS_OK;
+}
+
+vs_status vs_destroy(vs_handle A) {
+  if (!A) return VS_OK;
+  cudaDeviceSynchronize();
+  free_matrix(A->A);
+  if (A->T) {
+    free_matrix(*A->T);
+    delete A->T;
+  }
+  A->tp_partials.release();
+  A->tp_table.release();
+  A->stage_B.release();
+  A->stage_out.release();
+  delete A;
+  return VS_OK;
+}
+
+const char *vs_status_string(vs_status s) {
+  switch (s) {
+    case VS_OK: return "ok";
+    case VS_ERR_INVALID: return "invalid argument";
+    case VS_ERR_SHAPE: return "shape mismatch";
+    case VS_ERR_LAYOUT: return "unsupported operand layout";
+    case VS_ERR_RANGE: return "coordinate out of range";
+    case VS_ERR_ALLOC: return "allocation failed";
+    case VS_ERR_CUDA: return "CUDA error";
+    case VS_ERR_TIMEOUT: return "device wait timed out";
+    case VS_ERR_UNSUPPORTED: return "unsupported";
+    case VS_ERR_NAN: return "NaN value";
+  }
+  return "unknown status";
+}
+
+const char *vs_last_error(void) { return last_error(); }
+
+int32_t vs_version(void) { return 100; }
+
+}  // extern "C"

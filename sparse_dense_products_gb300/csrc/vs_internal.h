@@ -1,0 +1,146 @@
+// vs_internal.h -- handle layout, status helpers and launcher declarations
+// shared by the translation units of libvs.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/vs.h"
+
+namespace vs {
+
+// ------------------------------------------------------------------ errors
+
+void set_error(const std::string &msg);
+const char *last_error();
+
+struct Err {
+  vs_status code;
+  std::string msg;
+};
+
+// Returns VS_ERR_CUDA (with the message) if the last CUDA call failed.
+vs_status cuda_status(cudaError_t e, const char *what);
+
+#define VS_CUDA(call)                                          \
+  do {                                                         \
+    cudaError_t e_ = (call);                                   \
+    if (e_ != cudaSuccess) return ::vs::cuda_status(e_, #call); \
+  } while (0)
+
+#define VS_TRY(call)                 \
+  do {                               \
+    vs_status s_ = (call);           \
+    if (s_ != VS_OK) return s_;      \
+  } while (0)
+
+// ------------------------------------------------------------------ layout
+
+// Chunk length L: slices longer than L entries are split into chunks of L
+// entries, combined in chunk order.  A constant, so the summation order of a
+// product depends on the matrix only.
+constexpr int kChunkLen = 1024;
+
+// Widest column block one kernel launch handles; wider products loop.
+constexpr int kMaxBlockWidth = 64;
+
+// One stored layout of a matrix: CSR/CSC or VCSR/VCSC.
+struct Matrix {
+  vs_layout layout = VS_LAYOUT_CSR;
+  vs_major major = VS_MAJOR_ROW;
+  vs_dtype dtype = VS_F32;
+  int64_t n_rows = 0, n_cols = 0;
+  int64_t n_major = 0, n_minor = 0;
+  int64_t nnz = 0;
+  int64_t R = 0;  // VCS runs (CSR: nnz)
+
+  int32_t *ptr = nullptr;   // [n_major+1]  CSR slice starts / VCS run starts
+  int32_t *idx = nullptr;   // [nnz]        minor indices
+  void *vals = nullptr;     // CSR: [nnz] of dtype; VCS: [R] float32
+  int32_t *vptr = nullptr;  // VCS: [R+1]  index starts of the runs
+
+  // Matrix-only kernel parameters.
+  int g = 1;                    // group size: threads per slice (power of 2 in [1, 32])
+  int L = kChunkLen;            // chunk length
+  int64_t n_long = 0;           // slices longer than L
+  int64_t n_chunks = 0;         // chunks over all long slices
+  int4 *chunk_tasks = nullptr;  // [n_chunks] {slice, chunk k, long id, first partial}
+  int *counters = nullptr;      // [n_long] arrival counters (always left at 0)
+  void *partials = nullptr;     // [n_chunks * kMaxBlockWidth] of dtype
+  bool sorted_segments = false; // minor indices ascend inside every run / row
+
+  // Two-phase (deterministic misaligned) chunking of the slices: matrix-only.
+  int tp_chunks = 0;                // C
+  int32_t *tp_bounds = nullptr;     // [C+1] slice boundaries, balanced by entries
+
+  size_t dsize() const { return dtype == VS_F64 ? 8 : 4; }
+  int64_t layout_bytes() const;
+  int64_t meta_bytes() const;
+};
+
+// Scratch that grows on demand, owned by a handle.
+struct Scratch {
+  void *p = nullptr;
+  size_t bytes = 0;
+  vs_status reserve(size_t need, cudaStream_t s);
+  void release();
+};
+
+void free_matrix(Matrix &m);
+
+}  // namespace vs
+
+struct vs_handle_s {
+  vs::Matrix A;
+  vs::Matrix *T = nullptr;  // exact transpose (other major), once attached
+  int device = 0;
+  vs::Scratch tp_partials;   // two-phase chunk partials
+  vs::Scratch tp_table;      // two-phase tile offsets
+  vs::Scratch stage_B, stage_out;  // host-operand staging (vs_spmm_host)
+};
+
+namespace vs {
+
+// ------------------------------------------------------------------ builders (assembly.cu)
+
+// Builds a CSR/CSC (layout CSR) or VCSR/VCSC (layout VCS) from device COO.
+// `major_idx` / `minor_idx` are the COO coordinates along the major / minor
+// axis.  Fills `m` (device arrays owned by m).  Synchronises `s`.
+vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dtype,
+                       int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
+                       const int32_t *d_col, const void *d_val, cudaStream_t s);
+
+// Builds the other-major layout of `src` into `dst` from src's own arrays.
+vs_status build_transpose(const Matrix &src, Matrix &dst, cudaStream_t s);
+
+// Fills the matrix-only kernel parameters of `m` (g, chunk tasks, two-phase
+// chunk bounds) from its device arrays.  Synchronises `s`.
+vs_status prepare_matrix(Matrix &m, cudaStream_t s);
+
+// ------------------------------------------------------------------ products
+
+// Dense operand in the slice frame: row r of X is the dense vector that pairs
+// with index r; Y likewise.  Strides in elements; the width axis is contiguous.
+struct DenseView {
+  void *p;
+  int64_t rows;
+  int64_t ld;
+};
+
+// Aligned gather: Y[s, 0:w] = sum over entries (t, a) of slice s of a * X[t, 0:w].
+vs_status launch_gather(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s);
+
+// Misaligned scatter with atomic adds into a zero-filled Y.
+vs_status launch_scatter_atomic(const Matrix &m, DenseView X, DenseView Y, int64_t w,
+                                cudaStream_t s);
+
+// Misaligned scatter, deterministic two-phase.
+vs_status launch_scatter_two_phase(vs_handle_s &h, const Matrix &m, DenseView X, DenseView Y,
+                                   int64_t w, cudaStream_t s);
+
+// Y[0:rows, 0:w] = 0 with row stride ld.
+vs_status launch_zero_fill(DenseView Y, int64_t w, size_t dsize, cudaStream_t s);
+
+}  // namespace vs
