@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark: the six sparse x dense products on the 60,000 x 2,000 count matrix.
+
+Workload ("main"): 60,000 x 2,000, about 6.02M nonzeros (row nnz NegBin(mean
+100, r=2), Zipf(1.1) columns, values 1+Geometric(0.5)), dense width 16, fp32,
+seeded synthetic data generated on the device.  One step = the six products
+VCSR@B, VCSC@B, B@VCSR, B@VCSC, CSR@B and B@CSR, each once, with the matrix
+handles already built (assembly is timed separately and reported).  The
+misaligned products run the default deterministic two-phase variant; the
+atomic and transposed variants are reported beside them.
+
+Metric: effective HBM GB/s = algorithmic bytes / device time, where the
+algorithmic bytes of a product are every array of the stored layout, the dense
+operand read once and the output written once.  L2 is flushed (a 512 MiB
+write) before every timed product; CUDA events bracket each product on the
+launching stream.
+
+``--impl reference`` times the float64 CPU oracle on the same workload and
+metric (the deliberately slow reference; host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SpMM ms/product & effective HBM GB/s (% of 8 TB/s), 60k×2k 6M nnz w=16"
+WORKLOAD = "main"
+WIDTH = 16
+PRODUCTS = [  # name, layout, major, direction
+    ("VCSR@B", "vcs", "row", "A@B"),
+    ("VCSC@B", "vcs", "col", "A@B"),
+    ("B@VCSR", "vcs", "row", "B@A"),
+    ("B@VCSC", "vcs", "col", "B@A"),
+    ("CSR@B", "csr", "row", "A@B"),
+    ("B@CSR", "csr", "row", "B@A"),
+]
+NOMINAL_HBM_GBS = 8000.0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_bytes(A, n_x_rows: int, n_y_rows: int, w: int, es: int = 4) -> int:
+    layout_bytes, _ = A.nbytes()
+    return int(layout_bytes + n_x_rows * w * es + n_y_rows * w * es)
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+
+def oracle_prepare(coo):
+    """The oracle's own layouts of the workload, expanded to triples (not timed)."""
+    import oracle
+
+    r, c, v = coo.rows.numpy(), coo.cols.numpy(), coo.vals.numpy()
+    trip = {}
+    trip[("vcs", "row")] = oracle.vcs_triples(True, *oracle.vcs_build(coo.n_rows, coo.n_cols, r, c, v))
+    trip[("vcs", "col")] = oracle.vcs_triples(False, *oracle.vcs_build(coo.n_cols, coo.n_rows, c, r, v))
+    p, i, vv = oracle.csr_build(coo.n_rows, coo.n_cols, r, c, v)
+    trip[("csr", "row")] = oracle.csr_triples(True, p, i, vv)
+    return trip
+
+
+def run_oracle_sample(trip, coo, Bab, Bba_rows, budget_s: float):
+    """Times the oracle's six products, repeated until `budget_s` seconds have passed."""
+    import numpy as np
+    import oracle
+
+    Bba = np.ascontiguousarray(Bba_rows.T)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        for _, layout, major, direction in PRODUCTS:
+            ti, tj, ta = trip[(layout, major)]
+            if direction == "A@B":
+                oracle.spmm_ab(coo.n_rows, coo.n_cols, ti, tj, ta, Bab)
+            else:
+                oracle.spmm_ba(coo.n_rows, coo.n_cols, ti, tj, ta, Bba)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return reps, time.perf_counter() - t0
+
+
+def layout_bytes_host(coo):
+    """Algorithmic bytes of the six products computed on the host (for the reference arm)."""
+    import numpy as np
+
+    r, c = coo.rows.numpy().astype(np.int64), coo.cols.numpy().astype(np.int64)
+    v = coo.vals.numpy()
+    nnz = r.size
+    runs_r = np.unique(np.stack([r, v.view(np.uint32).astype(np.int64)]), axis=1).shape[1]
+    runs_c = np.unique(np.stack([c, v.view(np.uint32).astype(np.int64)]), axis=1).shape[1]
+    vcsr = 4 * (coo.n_rows + 1) + 4 * nnz + 8 * runs_r + 4
+    vcsc = 4 * (coo.n_cols + 1) + 4 * nnz + 8 * runs_c + 4
+    csr = 4 * (coo.n_rows + 1) + 8 * nnz
+    w, es = WIDTH, 4
+    ab = (coo.n_cols + coo.n_rows) * w * es
+    ba = (coo.n_rows + coo.n_cols) * w * es
+    return [vcsr + ab, vcsc + ab, vcsr + ba, vcsc + ba, csr + ab, csr + ba]
+
+
+def reference_arm(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import numpy as np
+    from sparse_dense_products_gb300 import workloads as W
+    import oracle
+
+    oracle.build()
+    coo = W.make(WORKLOAD, seed=0)
+    Bab = W.dense(coo.n_cols, WIDTH, seed=1).double().numpy()
+    Bba_rows = W.dense(coo.n_rows, WIDTH, seed=2).double().numpy()
+    per = layout_bytes_host(coo)
+    total_bytes = sum(per)
+    trip = oracle_prepare(coo)
+    # warm-up steps, then timed steps; one step = the six oracle products
+    for _ in range(args.warmup):
+        run_oracle_sample(trip, coo, Bab, Bba_rows, 0.0)
+    reps, secs = 0, 0.0
+    for _ in range(args.steps):
+        r_, s_ = run_oracle_sample(trip, coo, Bab, Bba_rows, 0.0)
+        reps += r_
+        secs += s_
+    gbs = total_bytes * reps / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / reps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "main: 60000x2000 count matrix, 6.02M nnz, width 16, six products",
+                   "l2": "n/a (host)"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "full workload, six float64 oracle products per step"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def gpu_arm(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl")
+
+    from sparse_dense_products_gb300 import build as vs_build
+    vs_build.build()
+    import sparse_dense_products_gb300 as vs
+    from sparse_dense_products_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    coo = W.make(WORKLOAD, seed=0, device=dev)
+    n_rows, n_cols = coo.n_rows, coo.n_cols
+
+    # ---- assembly (timed, reported; not part of the step)
+    assembly = {}
+    handles = {}
+    for key, fn in ((("vcs", "row"), vs.build_vcs), (("vcs", "col"), vs.build_vcs),
+                    (("csr", "row"), vs.build_csr)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        handles[key] = fn(coo.rows, coo.cols, coo.vals, (n_rows, n_cols), key[1])
+        torch.cuda.synchronize()
+        assembly[f"{'V' if key[0] == 'vcs' else ''}CS{'R' if key[1] == 'row' else 'C'}"] = \
+            round((time.perf_counter() - t0) * 1e3, 3)
+    for h in handles.values():
+        h.attach_transpose()
+
+    Bab = W.dense(n_cols, WIDTH, seed=1, device=dev)          # A@B operand
+    Bt = W.dense(n_rows, WIDTH, seed=2, device=dev)           # B@A operand, stored transposed
+    outs = {}
+    for name, layout, major, direction in PRODUCTS:
+        outs[name] = vs.empty_out(handles[(layout, major)], WIDTH, direction)
+
+    def run(name, layout, major, direction, variant="deterministic"):
+        A = handles[(layout, major)]
+        B = Bab if direction == "A@B" else Bt.t()
+        return vs.spmm(A, B, direction, variant, out=outs[name])
+
+    nbytes = {}
+    for name, layout, major, direction in PRODUCTS:
+        A = handles[(layout, major)]
+        nx = n_cols if direction == "A@B" else n_rows
+        ny = n_rows if direction == "A@B" else n_cols
+        nbytes[name] = algorithmic_bytes(A, nx, ny, WIDTH)
+
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn, reps):
+        """Device ms of fn() per rep, L2 flushed before each rep (events after the flush)."""
+        evs = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        for p in PRODUCTS:
+            run(*p)
+    torch.cuda.synchronize()
+
+    # ---- timed steps (barrier + synchronize on both sides)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = vs.kernel_launches()
+    per = {name: [] for name, *_ in PRODUCTS}
+    with Clocks(local) as clk:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            for p in PRODUCTS:
+                per[p[0]].extend(timed(lambda p=p: run(*p), 1))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    launches = vs.kernel_launches() - launches0
+    if ws > 1:
+        dist.barrier()
+    ms_prod = {k: statistics.mean(v) for k, v in per.items()}
+    ms_step = sum(ms_prod.values())
+    step_bytes = sum(nbytes.values())
+    t_local = ms_step
+    if ws > 1:
+        t = torch.tensor([t_local], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    else:
+        t_max = t_local
+    value = step_bytes * ws / (t_max * 1e-3) / 1e9
+
+    # ---- variants of the misaligned products (reported, not in the step)
+    variants = {}
+    for name, layout, major, direction in PRODUCTS:
+        aligned = (direction == "A@B") == (major == "row")
+        if aligned:
+            continue
+        for variant in ("atomic", "transposed"):
+            ts = timed(lambda: run(name, layout, major, direction, variant), max(5, args.steps))
+            ms = statistics.mean(ts)
+            variants[f"{name}/{variant}"] = {"ms": round(ms, 5),
+                                             "GBs": round(nbytes[name] / ms / 1e6, 1)}
+
+    # ---- e2e through vs_spmm_host with pinned host buffers
+    Bab_h = Bab.cpu().pin_memory()
+    Bt_h = Bt.cpu().pin_memory()
+    outs_h = {name: vs.empty_out(handles[(l, m)], WIDTH, d, device="cpu", pin_memory=True)
+              for name, l, m, d in PRODUCTS}
+    h2d = d2h = 0
+    for name, layout, major, direction in PRODUCTS:
+        h2d += (n_cols if direction == "A@B" else n_rows) * WIDTH * 4
+        d2h += (n_rows if direction == "A@B" else n_cols) * WIDTH * 4
+    e2e_times = []
+    for it in range(args.warmup + args.steps):
+        tot = 0.0
+        for name, layout, major, direction in PRODUCTS:
+            flush.fill_(1.0)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            vs.spmm_host(handles[(layout, major)], Bab_h if direction == "A@B" else Bt_h.t(),
+                         direction, "deterministic", out=outs_h[name])
+            tot += time.perf_counter() - t0
+        if it >= args.warmup:
+            e2e_times.append(tot)
+    e2e_s = statistics.mean(e2e_times)
+    e2e_value = step_bytes * ws / e2e_s / 1e9
+
+    # ---- roofline of the dominant kernel
+    peak, peak_kind = _peaks()
+    dom = max(ms_prod, key=ms_prod.get)
+    achieved = nbytes[dom] / (ms_prod[dom] * 1e-3) / 1e9
+    products = {k: {"ms": round(ms_prod[k], 5), "GBs": round(nbytes[k] / ms_prod[k] / 1e6, 1),
+                    "frac_of_8TBs": round(nbytes[k] / ms_prod[k] / 1e6 / NOMINAL_HBM_GBS, 4),
+                    "bytes": nbytes[k]} for k in ms_prod}
+
+    # ---- CPU baseline: the float64 oracle on host cores (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.skip_cpu:
+        coo_h = coo.to("cpu")
+        reps, secs = run_oracle_sample(oracle_prepare(coo_h), coo_h, Bab.double().cpu().numpy(),
+                                       Bt.double().cpu().numpy(), args.cpu_seconds)
+        cpu = {"value": round(step_bytes * reps / secs / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"the six float64 oracle products on the full workload, {reps} pass(es), "
+                         f"{secs:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "main: 60000x2000 count matrix, %d nnz, width 16, six products "
+                               "(VCSR@B VCSC@B B@VCSR B@VCSC CSR@B B@CSR), deterministic" % coo.nnz,
+                   "l2": "flushed before every product (512 MiB write)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "ms_per_product": round(t_max / len(PRODUCTS), 5),
+        "frac_of_8TBs": round(value / ws / NOMINAL_HBM_GBS, 4),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
+        "clocks": clk.summary(),
+        "gpu_launches": launches,
+        "products": products,
+        "misaligned_variants": variants,
+        "assembly_ms": assembly,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for h in handles.values():
+        h.destroy()
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum seconds of oracle work for cpu_baseline")
+    ap.add_argument("--skip-cpu", action="store_true", help="omit the cpu_baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

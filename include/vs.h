@@ -226,6 +226,10 @@ const char *vs_last_error(void);
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int32_t vs_version(void);
 
+/* Number of kernels libvs has launched in this process so far (all devices,
+ * all handles); a benchmark reads it before and after a timed region. */
+int64_t vs_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -85,6 +85,8 @@ def load() -> ctypes.CDLL:
         lib.vs_last_error.restype = ctypes.c_char_p
         lib.vs_version.argtypes = []
         lib.vs_version.restype = ctypes.c_int32
+        lib.vs_kernel_launches.argtypes = []
+        lib.vs_kernel_launches.restype = ctypes.c_int64
         _lib = lib
         return lib
 

@@ -224,3 +224,8 @@ def spmm_host(A: SparseMatrix, B: torch.Tensor, direction: str = "A@B",
 
 def version() -> int:
     return int(L.load().vs_version())
+
+
+def kernel_launches() -> int:
+    """``vs_kernel_launches``: kernels libvs has launched in this process."""
+    return int(L.load().vs_kernel_launches())

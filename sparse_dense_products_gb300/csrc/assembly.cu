@@ -124,17 +124,17 @@ vs_status exclusive_scan(const int32_t *in, int32_t *out, int64_t n, cudaStream_
   const int64_t nb = (n + kTile - 1) / kTile;
   if (nb <= 1) {
     scan_apply_kernel<<<1, kThreads, 0, s>>>(in, n, nullptr, out);
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
     return VS_OK;
   }
   Temp sums(s), offs(s);
   VS_TRY(sums.alloc(sizeof(int32_t) * nb));
   VS_TRY(offs.alloc(sizeof(int32_t) * (nb + 1)));
   scan_reduce_kernel<<<(unsigned)nb, kThreads, 0, s>>>(in, n, sums.as<int32_t>());
-  VS_CUDA(cudaGetLastError());
+  VS_LAUNCH_CHECK();
   VS_TRY(exclusive_scan(sums.as<int32_t>(), offs.as<int32_t>(), nb, s));
   scan_apply_kernel<<<(unsigned)nb, kThreads, 0, s>>>(in, n, offs.as<int32_t>(), out);
-  VS_CUDA(cudaGetLastError());
+  VS_LAUNCH_CHECK();
   return VS_OK;
 }
 
@@ -226,11 +226,11 @@ vs_status radix_passes(const int32_t **perm, const uint32_t *key, int64_t n, int
     int32_t *dst = (*perm == buf0) ? buf1 : buf0;
     radix_hist_kernel<<<(unsigned)ntiles, kThreads, 0, s>>>(*perm, key, n, shift,
                                                             hist.as<int32_t>(), ntiles);
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
     VS_TRY(exclusive_scan(hist.as<int32_t>(), offs.as<int32_t>(), 256 * ntiles, s));
     radix_scatter_kernel<<<(unsigned)ntiles, kThreads, 0, s>>>(*perm, key, n, shift,
                                                                offs.as<int32_t>(), ntiles, dst);
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
     *perm = dst;
   }
   return VS_OK;
@@ -395,7 +395,7 @@ vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dty
     check_kernel<<<std::min<unsigned>(kGridCap, grid_for(nnz, 256)), 256, 0, s>>>(
         maj, mnr, vcs ? static_cast<const float *>(d_val) : nullptr, nnz, m.n_major, m.n_minor,
         vkey.as<uint32_t>(), checks.as<Checks>());
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
   }
   Checks ck{};
   VS_CUDA(cudaMemcpyAsync(&ck, checks.p, sizeof ck, cudaMemcpyDeviceToHost, s));
@@ -420,7 +420,7 @@ vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dty
     // minor first (unless the input already orders it), then value bits, then major
     if (ck.minor_unsorted && ck.lex_unsorted && nnz > 1) {
       copy_key_kernel<<<eg, 256, 0, s>>>(mnr, keybuf.as<uint32_t>(), nnz);
-      VS_CUDA(cudaGetLastError());
+      VS_LAUNCH_CHECK();
       VS_TRY(radix_passes(&perm, keybuf.as<uint32_t>(), nnz, 0,
                           bit_length((uint64_t)std::max<int64_t>(m.n_minor - 1, 0)),
                           b0.as<int32_t>(), b1.as<int32_t>(), s));
@@ -433,14 +433,14 @@ vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dty
     }
     if (nnz > 1 && (ck.major_unsorted || diff || (ck.minor_unsorted && ck.lex_unsorted))) {
       copy_key_kernel<<<eg, 256, 0, s>>>(maj, keybuf.as<uint32_t>(), nnz);
-      VS_CUDA(cudaGetLastError());
+      VS_LAUNCH_CHECK();
       VS_TRY(radix_passes(&perm, keybuf.as<uint32_t>(), nnz, 0,
                           bit_length((uint64_t)std::max<int64_t>(m.n_major - 1, 0)),
                           b0.as<int32_t>(), b1.as<int32_t>(), s));
     }
   } else if (ck.major_unsorted && nnz > 1) {
     copy_key_kernel<<<eg, 256, 0, s>>>(maj, keybuf.as<uint32_t>(), nnz);
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
     VS_TRY(radix_passes(&perm, keybuf.as<uint32_t>(), nnz, 0,
                         bit_length((uint64_t)std::max<int64_t>(m.n_major - 1, 0)),
                         b0.as<int32_t>(), b1.as<int32_t>(), s));
@@ -461,9 +461,9 @@ vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dty
       gather_entries_kernel<<<eg, 256, 0, s>>>(perm, mnr, static_cast<const uint32_t *>(d_val),
                                                (int)(dsize / 4), nnz, m.idx,
                                                static_cast<uint32_t *>(m.vals));
-      VS_CUDA(cudaGetLastError());
+      VS_LAUNCH_CHECK();
       count_kernel<<<eg, 256, 0, s>>>(maj, nnz, cnt.as<int32_t>());
-      VS_CUDA(cudaGetLastError());
+      VS_LAUNCH_CHECK();
     }
     VS_TRY(exclusive_scan(cnt.as<int32_t>(), m.ptr, m.n_major, s));
     m.R = nnz;
@@ -478,9 +478,9 @@ vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dty
   int32_t R = 0;
   if (nnz > 0) {
     gather_entries_kernel<<<eg, 256, 0, s>>>(perm, mnr, nullptr, 0, nnz, m.idx, nullptr);
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
     run_flag_kernel<<<eg, 256, 0, s>>>(perm, maj, vkey.as<uint32_t>(), nnz, flag.as<int32_t>());
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
     VS_TRY(exclusive_scan(flag.as<int32_t>(), run_id.as<int32_t>(), nnz, s));
     VS_CUDA(cudaMemcpyAsync(&R, run_id.as<int32_t>() + nnz, sizeof R, cudaMemcpyDeviceToHost, s));
     VS_CUDA(cudaStreamSynchronize(s));
@@ -494,10 +494,10 @@ vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dty
     run_fill_kernel<<<eg, 256, 0, s>>>(perm, maj, static_cast<const float *>(d_val),
                                        flag.as<int32_t>(), run_id.as<int32_t>(), nnz, m.vptr,
                                        static_cast<float *>(m.vals), cnt.as<int32_t>());
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
   }
   set_int_kernel<<<1, 1, 0, s>>>(m.vptr + R, (int32_t)nnz);
-  VS_CUDA(cudaGetLastError());
+  VS_LAUNCH_CHECK();
   VS_TRY(exclusive_scan(cnt.as<int32_t>(), m.ptr, m.n_major, s));
   VS_CUDA(cudaStreamSynchronize(s));
   return VS_OK;
@@ -539,14 +539,14 @@ vs_status build_transpose(const Matrix &src, Matrix &dst, cudaStream_t s) {
   if (src.layout == VS_LAYOUT_CSR) {
     if (src.n_major > 0) {
       expand_csr_kernel<<<g, 256, 0, s>>>(src.ptr, src.n_major, maj.as<int32_t>());
-      VS_CUDA(cudaGetLastError());
+      VS_LAUNCH_CHECK();
     }
   } else {
     VS_TRY(vals.alloc(sizeof(float) * (size_t)std::max<int64_t>(nnz, 1)));
     if (src.n_major > 0) {
       expand_vcs_kernel<<<g, 256, 0, s>>>(src.ptr, src.vptr, static_cast<const float *>(src.vals),
                                           src.n_major, maj.as<int32_t>(), vals.as<float>());
-      VS_CUDA(cudaGetLastError());
+      VS_LAUNCH_CHECK();
     }
     val_ptr = vals.p;
   }
@@ -599,10 +599,10 @@ vs_status prepare_matrix(Matrix &m, cudaStream_t s) {
     VS_CUDA(cudaMemsetAsync(flag.p, 0, sizeof(int), s));
     mark_starts_kernel<<<std::min<unsigned>(kGridCap, grid_for(m.n_major, 256)), 256, 0, s>>>(
         m.ptr, m.n_major, start.as<uint8_t>());
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
     unsorted_kernel<<<std::min<unsigned>(kGridCap, grid_for(m.nnz, 256)), 256, 0, s>>>(
         m.idx, start.as<uint8_t>(), m.nnz, flag.as<int>());
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
     VS_CUDA(cudaMemcpyAsync(&unsorted, flag.p, sizeof(int), cudaMemcpyDeviceToHost, s));
     VS_CUDA(cudaStreamSynchronize(s));
     m.sorted_segments = !unsorted;

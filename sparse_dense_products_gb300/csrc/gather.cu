@@ -353,7 +353,7 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     const int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
     if (blocks > 0) {
       k<<<(unsigned)blocks, kThreads, 0, s>>>(a);
-      VS_CUDA(cudaGetLastError());
+      VS_LAUNCH_CHECK();
     }
   }
   return VS_OK;

@@ -427,7 +427,7 @@ vs_status atomic_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     const int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
     if (blocks > 0) {
       k<<<(unsigned)blocks, kThreads, 0, s>>>(a);
-      VS_CUDA(cudaGetLastError());
+      VS_LAUNCH_CHECK();
     }
   }
   return VS_OK;
@@ -480,13 +480,13 @@ vs_status two_phase_typed(vs_handle_s &h, const Matrix &m, DenseView X, DenseVie
     }
     dim3 grid((unsigned)tiles, (unsigned)C);
     k<<<grid, kThreads, smem, s>>>(a);
-    VS_CUDA(cudaGetLastError());
+    VS_LAUNCH_CHECK();
     if (C > 1) {
       const int64_t total = n_t * wb;
       const unsigned blocks = (unsigned)std::min<int64_t>(152 * 8, (total + 255) / 256);
       combine_kernel<T><<<std::max(1u, blocks), 256, 0, s>>>(
           static_cast<const T *>(h.tp_partials.p), C, n_t * wb, n_t, wb, yp, Y.ld);
-      VS_CUDA(cudaGetLastError());
+      VS_LAUNCH_CHECK();
     }
   }
   return VS_OK;
@@ -507,7 +507,7 @@ vs_status launch_zero_fill(DenseView Y, int64_t w, size_t dsize, cudaStream_t s)
   } else {
     zero_fill_kernel<float><<<std::max(1u, blocks), 256, 0, s>>>(static_cast<float *>(Y.p), Y.rows, w, Y.ld);
   }
-  VS_CUDA(cudaGetLastError());
+  VS_LAUNCH_CHECK();
   return VS_OK;
 }
 

@@ -11,6 +11,7 @@
 //              Y[t]    += a * X[slice]          (scatter.cu)
 // ("Add CUDA transfer and matmul kernels for the normalized views", "The
 // kernels": the same two binary choices as the host kernels.)
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -22,7 +23,11 @@ namespace vs {
 
 namespace {
 thread_local std::string g_last_error;
-}
+std::atomic<int64_t> g_launches{0};
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+int64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 void set_error(const std::string &msg) { g_last_error = msg; }
 const char *last_error() { return g_last_error.c_str(); }
@@ -360,5 +365,7 @@ const char *vs_status_string(vs_status s) {
 const char *vs_last_error(void) { return last_error(); }
 
 int32_t vs_version(void) { return 100; }
+
+int64_t vs_kernel_launches(void) { return launch_count(); }
 
 }  // extern "C"

@@ -30,6 +30,15 @@ vs_status cuda_status(cudaError_t e, const char *what);
     if (e_ != cudaSuccess) return ::vs::cuda_status(e_, #call); \
   } while (0)
 
+// Counts one kernel launch and checks that it was accepted.
+void note_launch();
+int64_t launch_count();
+#define VS_LAUNCH_CHECK()                     \
+  do {                                        \
+    ::vs::note_launch();                      \
+    VS_CUDA(cudaGetLastError());              \
+  } while (0)
+
 #define VS_TRY(call)                 \
   do {                               \
     vs_status s_ = (call);           \
