@@ -98,9 +98,11 @@ typedef struct {
     int64_t n_rows, n_cols; /* matrix shape */
     int64_t nnz;            /* stored entries (explicit zeros and duplicates kept) */
     int64_t n_runs;         /* VCS: number of runs R; CSR: nnz */
-    int64_t chunk_len;      /* L: slices longer than L are split into chunks of L entries */
-    int64_t n_long_slices;  /* slices longer than L */
+    int64_t chunk_len;      /* L: a slice with more than L entries (VCS: or more than L/4
+                               runs) is "long" and is cut into chunks of at most L entries */
+    int64_t n_long_slices;  /* long slices */
     int64_t n_chunks;       /* chunks over all long slices */
+    int64_t n_blocks;       /* blocks the kernels stream (runs of short slices, or chunks) */
     int32_t has_transpose;  /* 1 once vs_attach_transpose succeeded */
     int32_t reserved;
 } vs_info_t;

@@ -39,7 +39,8 @@ class Info(ctypes.Structure):
                 ("group_size", ctypes.c_int32), ("n_rows", ctypes.c_int64),
                 ("n_cols", ctypes.c_int64), ("nnz", ctypes.c_int64), ("n_runs", ctypes.c_int64),
                 ("chunk_len", ctypes.c_int64), ("n_long_slices", ctypes.c_int64),
-                ("n_chunks", ctypes.c_int64), ("has_transpose", ctypes.c_int32),
+                ("n_chunks", ctypes.c_int64), ("n_blocks", ctypes.c_int64),
+                ("has_transpose", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
 
 

@@ -124,11 +124,11 @@ _TYPESTR = {torch.int32: "<i4", torch.float32: "<f4", torch.float64: "<f8"}
 
 
 class _DeviceArray:
-    """A read-only 1-D device array exposed through __cuda_array_interface__."""
+    """A 1-D device array exposed through __cuda_array_interface__ (copied, never written)."""
 
     def __init__(self, ptr: int, n: int, typestr: str):
         self.__cuda_array_interface__ = {"shape": (int(n),), "typestr": typestr,
-                                         "data": (int(ptr), True), "version": 3, "strides": None}
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
 
 
 def _coo_args(rows: torch.Tensor, cols: torch.Tensor, vals: torch.Tensor):

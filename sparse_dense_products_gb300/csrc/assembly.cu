@@ -447,7 +447,8 @@ vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dty
   }
 
   // ---- owned arrays: slice pointer and indices (padded for vector over-reads)
-  VS_TRY(dev_alloc((void **)&m.ptr, sizeof(int32_t) * (m.n_major + 1)));
+  VS_TRY(dev_alloc((void **)&m.ptr, sizeof(int32_t) * (m.n_major + 1 + 16)));
+  VS_CUDA(cudaMemsetAsync(m.ptr, 0, sizeof(int32_t) * (m.n_major + 1 + 16), s));
   VS_TRY(dev_alloc((void **)&m.idx, sizeof(int32_t) * (nnz + 16)));
   VS_CUDA(cudaMemsetAsync(m.idx, 0, sizeof(int32_t) * (nnz + 16), s));
   Temp cnt(s);
@@ -621,49 +622,116 @@ vs_status prepare_matrix(Matrix &m, cudaStream_t s) {
     while (g * 2 <= mean && g < 32) g *= 2;
   }
   m.g = g;
-  m.L = kChunkLen;
+  {
+    int dev = 0;
+    VS_CUDA(cudaGetDevice(&dev));
+    VS_CUDA(cudaDeviceGetAttribute(&m.n_sm, cudaDevAttrMultiProcessorCount, dev));
+  }
 
-  // chunk tasks of the long slices
-  std::vector<int4> tasks;
-  int64_t n_long = 0;
+  // ---- blocks: runs of short slices, and chunks of long slices
+  const bool vcs = m.layout == VS_LAYOUT_VCS;
+  auto runs_of = [&](int64_t sl) -> int64_t { return vcs ? ptr[sl + 1] - ptr[sl] : 0; };
+  std::vector<int4> desc;
+  auto push = [&](int4 x, int4 y, int4 z) {
+    desc.push_back(x);
+    desc.push_back(y);
+    desc.push_back(z);
+  };
+  int64_t n_long = 0, n_chunks = 0, n_shares = 0;
+  int64_t bs0 = -1, be = 0, br = 0;  // open slice block: first slice, entries, runs
+  auto close_slices = [&](int64_t s_end) {
+    if (bs0 < 0) return;
+    push(make_int4((int)bs0, (int)s_end, (int)entry(bs0), (int)entry(s_end)),
+         make_int4(vcs ? ptr[bs0] : 0, vcs ? ptr[s_end] : 0, 0, -1), make_int4(0, 0, 0, 0));
+    bs0 = -1;
+  };
   for (int64_t sl = 0; sl < m.n_major; ++sl) {
-    const int64_t len = entry(sl + 1) - entry(sl);
-    if (len <= m.L) continue;
-    const int64_t nch = (len + m.L - 1) / m.L;
-    const int64_t first = (int64_t)tasks.size();
-    for (int64_t k = 0; k < nch; ++k)
-      tasks.push_back(make_int4((int)sl, (int)k, (int)n_long, (int)first));
+    const int64_t len = entry(sl + 1) - entry(sl), nr = runs_of(sl);
+    const bool is_long = len > kBlockEntries || nr > kBlockRuns;
+    if (!is_long) {
+      if (bs0 >= 0 && (be + len > kBlockEntries || br + nr > kBlockRuns ||
+                       sl - bs0 + 1 > kBlockSlices))
+        close_slices(sl);
+      if (bs0 < 0) {
+        bs0 = sl;
+        be = br = 0;
+      }
+      be += len;
+      br += nr;
+      continue;
+    }
+    close_slices(sl);
+    // cut the long slice into chunks of at most kBlockEntries entries and kBlockRuns runs
+    std::vector<int4> ch;  // {e0, e1, r0, r1}
+    int64_t pos = entry(sl), r = vcs ? ptr[sl] : 0;
+    const int64_t end = entry(sl + 1);
+    while (pos < end) {
+      int64_t e1 = std::min<int64_t>(end, pos + kBlockEntries);
+      int64_t r_first = r, r_last = r;
+      if (vcs) {
+        while (r_first < ptr[sl + 1] - 1 && vptr[r_first + 1] <= pos) ++r_first;
+        r_last = r_first;
+        while (r_last + 1 < ptr[sl + 1] && vptr[r_last + 1] < e1) ++r_last;
+        if (r_last - r_first + 1 > kBlockRuns) {
+          r_last = r_first + kBlockRuns - 1;
+          e1 = vptr[r_last + 1];
+        }
+        r = r_last;
+      }
+      ch.push_back(make_int4((int)pos, (int)e1, (int)r_first, (int)(r_last + 1)));
+      pos = e1;
+    }
+    int64_t sh = n_shares;  // first share of this slice
+    int64_t slice_shares = 0;
+    for (size_t k2 = 0; k2 < ch.size(); ++k2)
+      slice_shares += (ch[k2].y - ch[k2].x + kShareEntries - 1) / kShareEntries;
+    for (size_t k2 = 0; k2 < ch.size(); ++k2) {
+      push(make_int4((int)sl, (int)k2, ch[k2].x, ch[k2].y),
+           make_int4(vcs ? ch[k2].z : 0, vcs ? ch[k2].w : 0, 1, (int)n_long),
+           make_int4((int)sh, (int)n_shares, (int)slice_shares, 0));
+      sh += (ch[k2].y - ch[k2].x + kShareEntries - 1) / kShareEntries;
+    }
+    n_chunks += (int64_t)ch.size();
+    n_shares += slice_shares;
     ++n_long;
   }
+  close_slices(m.n_major);
+  m.n_blocks = (int64_t)desc.size() / 3;
   m.n_long = n_long;
-  m.n_chunks = (int64_t)tasks.size();
-  if (m.n_chunks > 0) {
-    VS_TRY(dev_alloc((void **)&m.chunk_tasks, sizeof(int4) * m.n_chunks));
-    VS_CUDA(cudaMemcpyAsync(m.chunk_tasks, tasks.data(), sizeof(int4) * m.n_chunks,
+  m.n_chunks = n_chunks;
+  m.n_shares = n_shares;
+  if (m.n_blocks > 0) {
+    VS_TRY(dev_alloc((void **)&m.blocks, sizeof(int4) * desc.size()));
+    VS_CUDA(cudaMemcpyAsync(m.blocks, desc.data(), sizeof(int4) * desc.size(),
                             cudaMemcpyHostToDevice, s));
+  }
+  if (n_long > 0) {
     VS_TRY(dev_alloc((void **)&m.counters, sizeof(int) * n_long));
     VS_CUDA(cudaMemsetAsync(m.counters, 0, sizeof(int) * n_long, s));
-    VS_TRY(dev_alloc(&m.partials, m.dsize() * kMaxBlockWidth * m.n_chunks));
+    VS_TRY(dev_alloc(&m.partials, m.dsize() * kMaxBlockWidth * n_shares));
   }
+  VS_TRY(dev_alloc((void **)&m.err, sizeof(int)));
+  VS_CUDA(cudaMemsetAsync(m.err, 0, sizeof(int), s));
 
-  // two-phase chunking: C contiguous slice ranges with balanced entry counts.
+  // ---- two-phase groups: C groups of consecutive blocks, balanced by entries.
   // C depends on the matrix only; it is kept small when the scattered output
   // is large, so that C partial copies of it stay bounded (64 MiB at width 64).
   {
-    int64_t c_nnz = std::max<int64_t>(1, (m.nnz + 32767) / 32768);
+    const int64_t c_nnz = std::max<int64_t>(1, (m.nnz + 32767) / 32768);
     const int64_t out_row_bytes = (int64_t)m.dsize() * kMaxBlockWidth;
-    int64_t c_mem = std::max<int64_t>(1, (int64_t(1) << 26) / std::max<int64_t>(1, m.n_minor * out_row_bytes));
+    const int64_t c_mem =
+        std::max<int64_t>(1, (int64_t(1) << 26) / std::max<int64_t>(1, m.n_minor * out_row_bytes));
     int64_t C = std::min<int64_t>(std::min(c_nnz, c_mem), 256);
-    C = std::max<int64_t>(1, std::min<int64_t>(C, std::max<int64_t>(m.n_major, 1)));
+    C = std::max<int64_t>(1, std::min<int64_t>(C, std::max<int64_t>(m.n_blocks, 1)));
     std::vector<int32_t> bounds(C + 1);
     bounds[0] = 0;
-    int64_t sl = 0;
+    int64_t b = 0;
     for (int64_t c = 1; c < C; ++c) {
       const int64_t target = m.nnz * c / C;
-      while (sl < m.n_major && entry(sl) < target) ++sl;
-      bounds[c] = (int32_t)sl;
+      while (b < m.n_blocks && desc[3 * b].z < target) ++b;
+      bounds[c] = (int32_t)b;
     }
-    bounds[C] = (int32_t)m.n_major;
+    bounds[C] = (int32_t)m.n_blocks;
     m.tp_chunks = (int)C;
     VS_TRY(dev_alloc((void **)&m.tp_bounds, sizeof(int32_t) * (C + 1)));
     VS_CUDA(cudaMemcpyAsync(m.tp_bounds, bounds.data(), sizeof(int32_t) * (C + 1),

@@ -1,7 +1,7 @@
 // gather.cu -- the aligned direction: Y[s, :] = sum over the entries (t, a)
-// of major slice s of a * X[t, :].  Covers CSR@B, VCSR@B, B@VCSC and CSC@B'
-// (through the transpose identity the caller maps every aligned product onto
-// this slice frame).
+// of major slice s of a * X[t, :].  Covers CSR@B, VCSR@B, B@VCSC and B@CSC
+// (every aligned product maps onto this slice frame, see vs_api.cu), and the
+// misaligned products run over an attached exact transpose.
 //
 // "Add CUDA transfer and matmul kernels for the normalized views", "The
 // kernels": one warp per major slice, lanes split between the dense width and
@@ -12,137 +12,60 @@
 // two, capped at a warp), summed in a fixed tree, so a product repeats exactly
 // and a column gives the same numbers alone or in a batch.
 //
-// The summation order of one output element (s, c) is fixed by the matrix:
-//   * logical partial k (0 <= k < g) sums, with fused multiply-adds in entry
-//     order, the entries n of the slice (or chunk) with (n - start) mod g == k;
-//   * the g partials meet in the butterfly p[k] += p[k + h] for
-//     h = g/2, g/4, ..., 1;
-//   * a slice longer than L entries is cut into chunks of L; chunk results are
-//     added in chunk order ((c0 + c1) + c2) + ... by the last chunk to finish.
+// Summation order of one output element (s, c), fixed by the matrix alone:
+//   * a run of entries (a whole short slice, or one warp's share of a chunk
+//     of a long slice) is summed as g logical partials -- partial k takes the
+//     entries n with (n - start) mod g == k, with fused multiply-adds in entry
+//     order -- which meet in the butterfly p[k] += p[k + h], h = g/2, ..., 1;
+//   * a long slice is cut into chunks (at most kBlockEntries entries and
+//     kBlockRuns runs, cut points fixed by the matrix) and every chunk into
+//     shares of kShareEntries entries; each share is one such run, and the
+//     share results are added in share order ((p0 + p1) + p2) + ... by the
+//     last share of the slice to finish.
 // Physically a lane holds NP = g / G of the logical partials (G slots per
 // slice, Q lanes per slot across the width); in-lane adds then shuffles
 // reproduce the same tree for every width, so bits never depend on w.
+//
+// Data movement: entries, values, slice pointers and runs arrive in shared
+// memory by bulk copies through a 4-deep ring fed by a producer warp
+// (stage.cuh); the dense rows X[t, :] are gathered through L1 with 16-byte
+// vector loads.
 #include <algorithm>
 
-#include "device_utils.cuh"
-#include "vs_internal.h"
+#include "stage.cuh"
 
 namespace vs {
 namespace {
 
-constexpr int kThreads = 256;
-
 struct GatherArgs {
-  const int32_t *ptr;   // [n_major+1]
-  const int32_t *idx;   // [nnz]
-  const void *vals;     // CSR: [nnz] of T; VCS: [R] float
-  const int32_t *vptr;  // VCS: [R+1]
+  StageArrays st;
   const void *X;
   int64_t ldx;
   void *Y;
   int64_t ldy;
-  int n_major;
-  int w;      // columns in this block (<= kMaxBlockWidth)
-  int G;      // physical slots per slice (g / NP)
-  int S;      // slices per warp in the regular part
-  int L;      // chunk length
-  int n_chunk_tasks;
-  const int4 *tasks;  // {slice, chunk k, long id, first partial}
-  void *partials;     // [n_chunks][kMaxBlockWidth] of T
-  int *counters;      // [n_long]
+  int w;          // columns in this block (<= kMaxBlockWidth)
+  int G;          // physical slots per slice (g / NP)
+  int S;          // slices per warp task
+  void *partials; // [n_shares][kMaxBlockWidth] of T
+  int *counters;  // [n_long]
 };
 
-template <bool VCS>
-__device__ __forceinline__ void slice_range(const GatherArgs &a, int s, int &e0, int &e1, int &rlo,
-                                            int &rhi) {
-  if (VCS) {
-    rlo = a.ptr[s];
-    rhi = a.ptr[s + 1];
-    e0 = a.vptr[rlo];
-    e1 = a.vptr[rhi];
-  } else {
-    rlo = rhi = 0;
-    e0 = a.ptr[s];
-    e1 = a.ptr[s + 1];
-  }
-}
-
-// VEC: elements per vector access; Q: lanes per slot; NP: logical partials per
-// lane; CI: column vectors per lane; VCS: layout.
+// Sums entries [n0, n1) of one slice into acc (logical partial (n - n0) mod g
+// lives in lane slot (n - n0) mod G, register (n - n0) / G mod NP), then runs
+// the fixed tree.  (VCS entries carry their run's value, expanded on chip.)
 template <typename T, int VEC, int Q, int NP, int CI, bool VCS>
-__global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
+__device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const T *__restrict__ X,
+                                             int64_t ldx, int n0, int n1, int G,
+                                             int slot, const int (&col0)[CI],
+                                             const bool (&colok)[CI], T (&acc)[NP][CI][VEC]) {
   using V = typename VecT<T, VEC>::type;
   using Ops = VecOps<T, VEC>;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const int G = a.G;
-  const int ql = lane & (Q - 1);
-  const int slot = (lane / Q) & (G - 1);
-  const int sub = lane / (Q * G);
-
-  int slice = -1, n0 = 0, n1 = 0, rlo = 0, rhi = 0, nch = 0;
-  const bool chunk = warp < a.n_chunk_tasks;
-  int4 task = make_int4(0, 0, 0, 0);
-  if (chunk) {
-    task = a.tasks[warp];
-    int e0, e1;
-    slice_range<VCS>(a, task.x, e0, e1, rlo, rhi);
-    nch = (e1 - e0 + a.L - 1) / a.L;
-    if (sub == 0) {
-      slice = task.x;
-      n0 = e0 + task.y * a.L;
-      n1 = min(e1, n0 + a.L);
-    }
-  } else {
-    const int64_t s = (warp - a.n_chunk_tasks) * a.S + sub;
-    if (s < a.n_major) {
-      int e0, e1;
-      slice_range<VCS>(a, (int)s, e0, e1, rlo, rhi);
-      if (e1 - e0 <= a.L) {  // longer slices belong to chunk tasks
-        slice = (int)s;
-        n0 = e0;
-        n1 = e1;
-      }
-    }
-  }
-
-  const T *__restrict__ X = static_cast<const T *>(a.X);
-  const T *__restrict__ vals = static_cast<const T *>(a.vals);
-  const float *__restrict__ rvals = static_cast<const float *>(a.vals);
-
-  T acc[NP][CI][VEC];
 #pragma unroll
   for (int i = 0; i < NP; ++i)
 #pragma unroll
     for (int ci = 0; ci < CI; ++ci)
 #pragma unroll
       for (int e = 0; e < VEC; ++e) acc[i][ci][e] = T(0);
-
-  bool colok[CI];
-  int col0[CI];
-#pragma unroll
-  for (int ci = 0; ci < CI; ++ci) {
-    col0[ci] = (ci * Q + ql) * VEC;
-    colok[ci] = col0[ci] < a.w;
-  }
-
-  // VCS: the run holding the lane's current entry
-  int r = 0, rend = 0;
-  T v = T(0);
-  if (VCS) {
-    const int n = n0 + slot;
-    if (n < n1) {
-      int lo = rlo, hi = rhi - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.vptr[mid] <= n) lo = mid;
-        else hi = mid - 1;
-      }
-      r = lo;
-      rend = a.vptr[r + 1];
-      v = (T)rvals[r];
-    }
-  }
 
   const int step = G * NP;
   for (int base = n0 + slot; base < n1; base += step) {
@@ -153,22 +76,8 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
     for (int i = 0; i < NP; ++i) {
       const int n = base + i * G;
       ok[i] = n < n1;
-      j[i] = ok[i] ? ld_stream(a.idx + n) : 0;
-      if (!VCS) av[i] = ok[i] ? ld_stream(vals + n) : T(0);
-    }
-    if (VCS) {
-#pragma unroll
-      for (int i = 0; i < NP; ++i) {
-        const int n = base + i * G;
-        if (ok[i] && n >= rend) {
-          do {
-            ++r;
-            rend = a.vptr[r + 1];
-          } while (n >= rend);
-          v = (T)rvals[r];
-        }
-        av[i] = v;
-      }
+      j[i] = ok[i] ? sv.idx[n] : 0;
+      av[i] = ok[i] ? sv.vals[n] : T(0);
     }
     V x[NP][CI];
 #pragma unroll
@@ -176,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
 #pragma unroll
       for (int ci = 0; ci < CI; ++ci)
         if (ok[i] && colok[ci])
-          x[i][ci] = ld_gather(reinterpret_cast<const V *>(X + (int64_t)j[i] * a.ldx + col0[ci]));
+          x[i][ci] = ld_gather(reinterpret_cast<const V *>(X + (int64_t)j[i] * ldx + col0[ci]));
 #pragma unroll
     for (int i = 0; i < NP; ++i)
 #pragma unroll
@@ -188,8 +97,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
           for (int e = 0; e < VEC; ++e) acc[i][ci][e] = fma(av[i], xe[e], acc[i][ci][e]);
         }
   }
-
-  // fixed tree: in-lane levels (strides h*G), then across slots (strides < G)
+  // the fixed tree: in-lane levels (strides h*G), then across slots (strides < G)
 #pragma unroll
   for (int h = NP / 2; h >= 1; h >>= 1)
 #pragma unroll
@@ -204,51 +112,104 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
 #pragma unroll
       for (int e = 0; e < VEC; ++e)
         acc[0][ci][e] = acc[0][ci][e] + __shfl_xor_sync(kFullMask, acc[0][ci][e], sft * Q);
+}
 
-  T *__restrict__ Y = static_cast<T *>(a.Y);
-  if (!chunk) {
-    if (slice >= 0 && slot == 0) {
-#pragma unroll
-      for (int ci = 0; ci < CI; ++ci)
-        if (colok[ci])
-          *reinterpret_cast<V *>(Y + (int64_t)slice * a.ldy + col0[ci]) = Ops::pack(acc[0][ci]);
-    }
+template <typename T, int VEC, int Q, int NP, int CI, bool VCS>
+__global__ void __launch_bounds__(kPipeThreads, 2) gather_kernel(const GatherArgs a) {
+  using V = typename VecT<T, VEC>::type;
+  using Ops = VecOps<T, VEC>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Pipe<T, VCS> pipe{smem};
+  pipe.init();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (wid == kWarpsPerCta) {  // the producer warp
+    pipe.produce(a.st, blockIdx.x, a.st.n_blocks, gridDim.x);
     return;
   }
+  const int G = a.G;
+  const int ql = lane & (Q - 1);
+  const int slot = (lane / Q) & (G - 1);
+  const int sub = lane / (Q * G);
+  const T *__restrict__ X = static_cast<const T *>(a.X);
+  T *__restrict__ Y = static_cast<T *>(a.Y);
+  int col0[CI];
+  bool colok[CI];
+#pragma unroll
+  for (int ci = 0; ci < CI; ++ci) {
+    col0[ci] = (ci * Q + ql) * VEC;
+    colok[ci] = col0[ci] < a.w;
+  }
 
-  // chunk of a long slice: publish the partial, the last chunk to arrive combines
-  T *__restrict__ P = static_cast<T *>(a.partials);
-  if (slice >= 0 && slot == 0) {
+  int i = 0;
+  for (int b = blockIdx.x; b < a.st.n_blocks; b += gridDim.x, ++i) {
+    if (!pipe.acquire(i, a.st)) return;
+    const Block k = load_block(a.st.blocks, b);
+    const Staged<T, VCS> sv = stage_views<T, VCS>(k, pipe.buf(i % kStages));
+    const int units = block_units(k, a.S);
+    T acc[NP][CI][VEC];
+    for (int u = pipe.grab(i); u < units; u = pipe.grab(i)) {
+      if (k.type == 0) {
+        // ---- S consecutive slices, one per sub-group
+        if (VCS) {
+          const int sa = k.s0 + u * a.S, sb = min(k.s1, sa + a.S);
+          expand_runs<T, VCS>(k, pipe.buf(i % kStages), sv.vptr[sv.ptr[sa]], sv.vptr[sv.ptr[sb]],
+                              sv.ptr[sa], sv.ptr[sb]);
+        }
+        const int s = k.s0 + u * a.S + sub;
+        const bool mine = s < k.s1;
+        int n0 = 0, n1 = 0;
+        if (mine) {
+          if (VCS) {
+            n0 = sv.vptr[sv.ptr[s]];
+            n1 = sv.vptr[sv.ptr[s + 1]];
+          } else {
+            n0 = sv.ptr[s];
+            n1 = sv.ptr[s + 1];
+          }
+        }
+        gather_range<T, VEC, Q, NP, CI, VCS>(sv, X, a.ldx, n0, n1, G, slot, col0, colok, acc);
+        if (mine && slot == 0) {
 #pragma unroll
-    for (int ci = 0; ci < CI; ++ci)
-      if (colok[ci])
-        *reinterpret_cast<V *>(P + (int64_t)(task.w + task.y) * kMaxBlockWidth + col0[ci]) =
-            Ops::pack(acc[0][ci]);
-  }
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  if (lane == 0) last = atomicAdd(a.counters + task.z, 1) == nch - 1;
-  last = __shfl_sync(kFullMask, last, 0);
-  if (!last) return;
-  __threadfence();
-  if (sub == 0 && slot == 0) {
+          for (int ci = 0; ci < CI; ++ci)
+            if (colok[ci])
+              *reinterpret_cast<V *>(Y + (int64_t)s * a.ldy + col0[ci]) = Ops::pack(acc[0][ci]);
+        }
+      } else {
+        // ---- share u of a chunk of a long slice: publish its partial; the last
+        // share of the slice to arrive adds all of them in share order
+        if (VCS)
+          expand_runs<T, VCS>(k, pipe.buf(i % kStages), k.e0 + u * kShareEntries,
+                              min(k.e1, k.e0 + (u + 1) * kShareEntries), k.r0, k.r1);
+        const int n0 = sub == 0 ? k.e0 + u * kShareEntries : 0;
+        const int n1 = sub == 0 ? min(k.e1, n0 + kShareEntries) : 0;
+        gather_range<T, VEC, Q, NP, CI, VCS>(sv, X, a.ldx, n0, n1, G, slot, col0, colok, acc);
+        T *__restrict__ P = static_cast<T *>(a.partials);
+        if (sub == 0 && slot == 0) {
 #pragma unroll
-    for (int ci = 0; ci < CI; ++ci) {
-      if (!colok[ci]) continue;
-      T sum[VEC];
-      for (int k = 0; k < nch; ++k) {
-        const V pv = __ldcg(reinterpret_cast<const V *>(P + (int64_t)(task.w + k) * kMaxBlockWidth +
-                                                         col0[ci]));
-        T pe[VEC];
-        Ops::unpack(pv, pe);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) sum[e] = k == 0 ? pe[e] : sum[e] + pe[e];
+          for (int ci = 0; ci < CI; ++ci)
+            if (colok[ci])
+              *reinterpret_cast<V *>(P + (int64_t)(k.first + u) * kMaxBlockWidth + col0[ci]) =
+                  Ops::pack(acc[0][ci]);
+        }
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(a.counters + k.lid, 1) == k.nsh - 1;
+        last = __shfl_sync(kFullMask, last, 0);
+        if (last) {
+          __threadfence();
+          for (int c = lane; c < a.w; c += 32) {
+            T sum = __ldcg(P + (int64_t)k.sfirst * kMaxBlockWidth + c);
+            for (int q = 1; q < k.nsh; ++q)
+              sum = sum + __ldcg(P + (int64_t)(k.sfirst + q) * kMaxBlockWidth + c);
+            Y[(int64_t)k.s0 * a.ldy + c] = sum;
+          }
+          if (lane == 0) a.counters[k.lid] = 0;  // re-armed for the next launch
+        }
       }
-      *reinterpret_cast<V *>(Y + (int64_t)task.x * a.ldy + col0[ci]) = Ops::pack(sum);
     }
+    pipe.release(i);
   }
-  if (lane == 0) a.counters[task.z] = 0;  // re-armed for the next launch
 }
 
 // ------------------------------------------------------------------ dispatch
@@ -303,6 +264,7 @@ inline int pow2ceil(int x) {
 template <typename T, bool VCS>
 vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s) {
   constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
+  constexpr int smem = pipe_smem_bytes<T, VCS>(0);
   for (int64_t c0 = 0; c0 < w; c0 += kMaxBlockWidth) {
     const int wb = (int)std::min<int64_t>(kMaxBlockWidth, w - c0);
     const T *xp = static_cast<const T *>(X.p) + c0;
@@ -332,27 +294,23 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
       return VS_ERR_UNSUPPORTED;
     }
     GatherArgs a;
-    a.ptr = m.ptr;
-    a.idx = m.idx;
-    a.vals = m.vals;
-    a.vptr = m.vptr;
+    a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
+                       nullptr, 0, 0, 0};
     a.X = xp;
     a.ldx = X.ld;
     a.Y = yp;
     a.ldy = Y.ld;
-    a.n_major = (int)m.n_major;
     a.w = wb;
     a.G = G;
     a.S = 32 / (Q * G);
-    a.L = m.L;
-    a.n_chunk_tasks = (int)m.n_chunks;
-    a.tasks = m.chunk_tasks;
     a.partials = m.partials;
     a.counters = m.counters;
-    const int64_t warps = m.n_chunks + (m.n_major + a.S - 1) / a.S;
-    const int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
-    if (blocks > 0) {
-      k<<<(unsigned)blocks, kThreads, 0, s>>>(a);
+    int per_sm = 0;
+    VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kPipeThreads, smem));
+    const int64_t grid = std::min<int64_t>(m.n_blocks, (int64_t)std::max(1, per_sm) * m.n_sm);
+    if (grid > 0) {
+      k<<<(unsigned)grid, kPipeThreads, smem, s>>>(a);
       VS_LAUNCH_CHECK();
     }
   }

@@ -3,156 +3,140 @@
 //
 // "Add CUDA transfer and matmul kernels for the normalized views", "The
 // kernels": the misaligned directions add into the output with atomics, which
-// makes them nondeterministic in the last bits.  Two schemes live here:
+// makes them nondeterministic in the last bits.  Two schemes live here, both
+// fed by the block stream of stage.cuh (entries arrive in shared memory by
+// bulk copies, a block ahead):
 //
-//  * atomic: zero-fill Y, then each warp takes a slice (or a chunk of a long
-//    slice), loads X[s, :] once and adds a * X[s, :] into row t with vector
-//    reductions (red.global.add.v4.f32).
+//  * atomic: zero-fill Y, then warps take slices (or shares of a chunk of a
+//    long slice), load X[s, :] once and add a * X[s, :] into row t with
+//    vector reductions (red.global.add.v4.f32).
 //
-//  * two-phase (deterministic): the slices are cut into C contiguous chunks
-//    (balanced by entries, C fixed by the matrix) and Y into tiles of rows
-//    that fit in shared memory.  Phase 1: block (tile, chunk) accumulates, in
-//    slice order and entry order, the chunk's contributions to its tile in
-//    shared memory; each warp owns a band of the tile's rows, so no two
-//    threads ever update one element concurrently.  Phase 2 adds the C chunk
-//    partials of every element in chunk order.  The order of every element's
-//    sum therefore depends on the matrix alone.
+//  * two-phase (deterministic): the blocks are cut into C consecutive groups
+//    (balanced by entries, C fixed by the matrix) and Y into tiles of rows that
+//    fit in shared memory.  Phase 1: CTA (tile, group) streams its group's
+//    blocks in order and accumulates, in slice order and entry order, the
+//    contributions that land in its tile; each warp owns a band of the tile's
+//    rows, so no two threads update one element concurrently, and duplicate
+//    rows met together are applied one after another in entry order.  Phase 2
+//    adds the C group partials of every element in group order.  The order of
+//    every element's sum therefore depends on the matrix alone.
 #include <algorithm>
 
-#include "device_utils.cuh"
-#include "vs_internal.h"
+#include "stage.cuh"
 
 namespace vs {
 namespace {
 
-constexpr int kThreads = 256;
-
 __device__ __forceinline__ float fma_t(float a, float b, float c) { return fmaf(a, b, c); }
 __device__ __forceinline__ double fma_t(double a, double b, double c) { return fma(a, b, c); }
 
+// ------------------------------------------------------------------ atomic
+
 struct ScatterArgs {
-  const int32_t *ptr;
-  const int32_t *idx;
-  const void *vals;
-  const int32_t *vptr;
+  StageArrays st;
   const void *X;
   int64_t ldx;
   void *Y;
   int64_t ldy;
-  int n_major;
   int w;
   int G;  // slots per slice
-  int S;  // slices per warp
-  int L;
-  int n_chunk_tasks;
-  const int4 *tasks;
+  int S;  // slices per warp task
 };
 
-template <bool VCS, typename A>
-__device__ __forceinline__ void slice_range(const A &a, int s, int &e0, int &e1, int &rlo,
-                                            int &rhi) {
-  if (VCS) {
-    rlo = a.ptr[s];
-    rhi = a.ptr[s + 1];
-    e0 = a.vptr[rlo];
-    e1 = a.vptr[rhi];
-  } else {
-    rlo = rhi = 0;
-    e0 = a.ptr[s];
-    e1 = a.ptr[s + 1];
-  }
-}
-
-// ------------------------------------------------------------------ atomic
-
+// Entries [n0, n1) of slice s: Y[t, :] += a * x for each, slot-strided.
 template <typename T, int VEC, int Q, int CI, bool VCS>
-__global__ void __launch_bounds__(kThreads) scatter_atomic_kernel(const ScatterArgs a) {
-  using V = typename VecT<T, VEC>::type;
-  using Ops = VecOps<T, VEC>;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const int G = a.G;
-  const int ql = lane & (Q - 1);
-  const int slot = (lane / Q) & (G - 1);
-  const int sub = lane / (Q * G);
-
-  int slice = -1, n0 = 0, n1 = 0, rlo = 0, rhi = 0;
-  if (warp < a.n_chunk_tasks) {
-    const int4 task = a.tasks[warp];
-    int e0, e1;
-    slice_range<VCS>(a, task.x, e0, e1, rlo, rhi);
-    if (sub == 0) {
-      slice = task.x;
-      n0 = e0 + task.y * a.L;
-      n1 = min(e1, n0 + a.L);
-    }
-  } else {
-    const int64_t s = (warp - a.n_chunk_tasks) * a.S + sub;
-    if (s < a.n_major) {
-      int e0, e1;
-      slice_range<VCS>(a, (int)s, e0, e1, rlo, rhi);
-      if (e1 - e0 <= a.L) {
-        slice = (int)s;
-        n0 = e0;
-        n1 = e1;
-      }
-    }
-  }
-  if (slice < 0) return;
-
-  const T *__restrict__ X = static_cast<const T *>(a.X);
-  T *__restrict__ Y = static_cast<T *>(a.Y);
-  const T *__restrict__ vals = static_cast<const T *>(a.vals);
-  const float *__restrict__ rvals = static_cast<const float *>(a.vals);
-  T x[CI][VEC];
-  bool colok[CI];
-  int col0[CI];
-#pragma unroll
-  for (int ci = 0; ci < CI; ++ci) {
-    col0[ci] = (ci * Q + ql) * VEC;
-    colok[ci] = col0[ci] < a.w;
-    if (colok[ci]) Ops::unpack(ld_gather(reinterpret_cast<const V *>(X + (int64_t)slice * a.ldx + col0[ci])), x[ci]);
-  }
-  int r = 0, rend = 0;
-  T v = T(0);
-  if (VCS) {
-    const int n = n0 + slot;
-    if (n < n1) {
-      int lo = rlo, hi = rhi - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.vptr[mid] <= n) lo = mid;
-        else hi = mid - 1;
-      }
-      r = lo;
-      rend = a.vptr[r + 1];
-      v = (T)rvals[r];
-    }
-  }
+__device__ __forceinline__ void scatter_range(const Staged<T, VCS> &sv, const T (&x)[CI][VEC],
+                                              T *__restrict__ Y, int64_t ldy, int n0, int n1,
+                                              int G, int slot, const int (&col0)[CI],
+                                              const bool (&colok)[CI]) {
 #pragma unroll 4
   for (int n = n0 + slot; n < n1; n += G) {
-    const int t = ld_stream(a.idx + n);
-    T av;
-    if (VCS) {
-      if (n >= rend) {
-        do {
-          ++r;
-          rend = a.vptr[r + 1];
-        } while (n >= rend);
-        v = (T)rvals[r];
-      }
-      av = v;
-    } else {
-      av = ld_stream(vals + n);
-    }
+    const int t = sv.idx[n];
+    const T av = sv.vals[n];
 #pragma unroll
     for (int ci = 0; ci < CI; ++ci) {
       if (!colok[ci]) continue;
       T c[VEC];
 #pragma unroll
       for (int e = 0; e < VEC; ++e) c[e] = av * x[ci][e];
-      red_add(Y + (int64_t)t * a.ldy + col0[ci], c);
+      red_add(Y + (int64_t)t * ldy + col0[ci], c);
     }
+  }
+}
+
+template <typename T, int VEC, int Q, int CI, bool VCS>
+__global__ void __launch_bounds__(kPipeThreads) scatter_atomic_kernel(const ScatterArgs a) {
+  using V = typename VecT<T, VEC>::type;
+  using Ops = VecOps<T, VEC>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Pipe<T, VCS> pipe{smem};
+  pipe.init();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (wid == kWarpsPerCta) {  // the producer warp
+    pipe.produce(a.st, blockIdx.x, a.st.n_blocks, gridDim.x);
+    return;
+  }
+  const int G = a.G;
+  const int ql = lane & (Q - 1);
+  const int slot = (lane / Q) & (G - 1);
+  const int sub = lane / (Q * G);
+  const T *__restrict__ X = static_cast<const T *>(a.X);
+  T *__restrict__ Y = static_cast<T *>(a.Y);
+  int col0[CI];
+  bool colok[CI];
+#pragma unroll
+  for (int ci = 0; ci < CI; ++ci) {
+    col0[ci] = (ci * Q + ql) * VEC;
+    colok[ci] = col0[ci] < a.w;
+  }
+
+  int i = 0;
+  for (int b = blockIdx.x; b < a.st.n_blocks; b += gridDim.x, ++i) {
+    if (!pipe.acquire(i, a.st)) return;
+    const Block k = load_block(a.st.blocks, b);
+    const Staged<T, VCS> sv = stage_views<T, VCS>(k, pipe.buf(i % kStages));
+    const int units = block_units(k, a.S);
+    T x[CI][VEC];
+    for (int u = pipe.grab(i); u < units; u = pipe.grab(i)) {
+      int s, n0 = 0, n1 = 0;
+      if (VCS) {  // run values of this unit's entries, on chip
+        if (k.type == 0) {
+          const int sa = k.s0 + u * a.S, sb = min(k.s1, sa + a.S);
+          expand_runs<T, VCS>(k, pipe.buf(i % kStages), sv.vptr[sv.ptr[sa]], sv.vptr[sv.ptr[sb]],
+                              sv.ptr[sa], sv.ptr[sb]);
+        } else {
+          expand_runs<T, VCS>(k, pipe.buf(i % kStages), k.e0 + u * kShareEntries,
+                              min(k.e1, k.e0 + (u + 1) * kShareEntries), k.r0, k.r1);
+        }
+      }
+      if (k.type == 0) {
+        s = k.s0 + u * a.S + sub;
+        if (s < k.s1) {
+          if (VCS) {
+            n0 = sv.vptr[sv.ptr[s]];
+            n1 = sv.vptr[sv.ptr[s + 1]];
+          } else {
+            n0 = sv.ptr[s];
+            n1 = sv.ptr[s + 1];
+          }
+        }
+      } else {
+        s = k.s0;
+        if (sub == 0) {
+          n0 = k.e0 + u * kShareEntries;
+          n1 = min(k.e1, n0 + kShareEntries);
+        }
+      }
+      if (n0 < n1) {
+#pragma unroll
+        for (int ci = 0; ci < CI; ++ci)
+          if (colok[ci])
+            Ops::unpack(ld_gather(reinterpret_cast<const V *>(X + (int64_t)s * a.ldx + col0[ci])),
+                        x[ci]);
+        scatter_range<T, VEC, Q, CI, VCS>(sv, x, Y, a.ldy, n0, n1, G, slot, col0, colok);
+      }
+    }
+    pipe.release(i);
   }
 }
 
@@ -168,7 +152,6 @@ __global__ void zero_fill_kernel(T *__restrict__ Y, int64_t rows, int64_t w, int
   }
 }
 
-template <typename T>
 __global__ void zero_fill_vec_kernel(float4 *__restrict__ Y, int64_t n16) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
        i += (int64_t)gridDim.x * blockDim.x)
@@ -178,130 +161,171 @@ __global__ void zero_fill_vec_kernel(float4 *__restrict__ Y, int64_t n16) {
 // ------------------------------------------------------------------ two-phase
 
 struct TwoPhaseArgs {
-  const int32_t *ptr;
-  const int32_t *idx;
-  const void *vals;
-  const int32_t *vptr;
+  StageArrays st;
   const void *X;
   int64_t ldx;
-  void *out;      // Y (C == 1) or the chunk partials
-  int64_t ldo;    // row stride of `out`
-  int64_t part_stride;  // elements between chunk partials (C > 1)
-  const int32_t *bounds;  // [C+1] slice boundaries of the chunks
-  int64_t n_t;    // rows of Y
-  int tile_rows;  // rows per tile
+  void *out;              // Y (C == 1) or the group partials
+  int64_t ldo;            // row stride of `out`
+  int64_t part_stride;    // elements between group partials (C > 1)
+  const int32_t *bounds;  // [C+1] block boundaries of the groups
+  int64_t n_t;            // rows of Y
+  int tile_rows;          // rows per tile
   int w;
 };
 
-// Block (tile blockIdx.x, chunk blockIdx.y).  Shared memory: tile_rows x w of T.
 template <typename T, int VEC, int Q, int CI, bool VCS>
-__global__ void __launch_bounds__(kThreads) two_phase_kernel(const TwoPhaseArgs a) {
+struct TwoPhaseWarp {
   using V = typename VecT<T, VEC>::type;
   using Ops = VecOps<T, VEC>;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  T *tile = reinterpret_cast<T *>(smem_raw);
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  constexpr int NW = kThreads / 32;
-  constexpr int E = 32 / Q;  // entries handled per step
-  const int64_t t0 = (int64_t)blockIdx.x * a.tile_rows;
-  const int rows = (int)(a.n_t - t0 < a.tile_rows ? a.n_t - t0 : a.tile_rows);
-  const int band = (rows + NW - 1) / NW;
-  const int my_lo = wid * band, my_hi = min(rows, my_lo + band);  // tile-relative rows
-  const int w = a.w;
+  static constexpr int E = 32 / Q;  // entries applied per step
 
-  for (int i = threadIdx.x; i < rows * w; i += kThreads) tile[i] = T(0);
-  __syncthreads();
-
-  const T *__restrict__ X = static_cast<const T *>(a.X);
-  const T *__restrict__ vals = static_cast<const T *>(a.vals);
-  const float *__restrict__ rvals = static_cast<const float *>(a.vals);
-  const int ql = lane & (Q - 1), grp = lane / Q;
-  int col0[CI];
-  bool colok[CI];
+  __device__ __forceinline__ static void apply(T *tile, int w, int tk, T ak, const T (&x)[CI][VEC],
+                                               const int (&col0)[CI], const bool (&colok)[CI]) {
 #pragma unroll
-  for (int ci = 0; ci < CI; ++ci) {
-    col0[ci] = (ci * Q + ql) * VEC;
-    colok[ci] = col0[ci] < w;
+    for (int ci = 0; ci < CI; ++ci) {
+      if (!colok[ci]) continue;
+      V *p = reinterpret_cast<V *>(tile + (int64_t)tk * w + col0[ci]);
+      T cur[VEC];
+      Ops::unpack(*p, cur);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) cur[e] = fma_t(ak, x[ci][e], cur[e]);
+      *p = Ops::pack(cur);
+    }
   }
 
-  const int s_begin = a.bounds[blockIdx.y], s_end = a.bounds[blockIdx.y + 1];
-  if (my_lo < my_hi) {
-    for (int s = s_begin; s < s_end; ++s) {
-      int e0, e1, rlo, rhi;
-      slice_range<VCS>(a, s, e0, e1, rlo, rhi);
-      if (e0 == e1) continue;
-      T x[CI][VEC];
+  // Applies the entries [n0, n1) of slice s whose rows fall in this warp's
+  // band [lo, hi) (tile-relative), in entry order.
+  __device__ __forceinline__ static void run(const Staged<T, VCS> &sv, const T *__restrict__ X,
+                                             int64_t ldx, T *tile, int w, int64_t t0, int lo,
+                                             int hi, int s, int n0, int n1, int rlo, int rhi,
+                                             const int (&col0)[CI], const bool (&colok)[CI]) {
+    const int lane = threadIdx.x & 31, grp = lane / Q;
+    T x[CI][VEC];
 #pragma unroll
-      for (int ci = 0; ci < CI; ++ci)
-        if (colok[ci])
-          Ops::unpack(ld_gather(reinterpret_cast<const V *>(X + (int64_t)s * a.ldx + col0[ci])), x[ci]);
-      int r = rlo;  // VCS: run of this lane's entry (monotone in n)
-      for (int base = e0; base < e1; base += 32) {
-        const int n = base + lane;
-        int t = -1;
-        T av = T(0);
-        if (n < e1) {
-          const int tt = ld_stream(a.idx + n) - (int)t0;
-          if (tt >= my_lo && tt < my_hi) {
-            t = tt;
-            if (VCS) {
-              while (a.vptr[r + 1] <= n) ++r;
-              av = (T)rvals[r];
-            } else {
-              av = ld_stream(vals + n);
+    for (int ci = 0; ci < CI; ++ci)
+      if (colok[ci])
+        Ops::unpack(ld_gather(reinterpret_cast<const V *>(X + (int64_t)s * ldx + col0[ci])), x[ci]);
+    for (int base = n0; base < n1; base += 32) {
+      const int n = base + lane;
+      int t = -1;
+      T av = T(0);
+      if (n < n1) {
+        const int tt = (int)(sv.idx[n] - t0);
+        if (tt >= lo && tt < hi) {
+          t = tt;
+          if (VCS) {  // the run of entry n
+            int a0 = rlo, a1 = rhi - 1;
+            while (a0 < a1) {
+              const int mid = (a0 + a1 + 1) >> 1;
+              if (sv.vptr[mid] <= n) a0 = mid;
+              else a1 = mid - 1;
             }
+            av = (T)sv.rvals[a0];
+          } else {
+            av = sv.vals[n];
           }
         }
-        unsigned bits = __ballot_sync(kFullMask, t >= 0);
-        while (bits) {
-          // the k-th of the next E selected entries goes to lane group k, in entry order
-          const int cnt = min(E, __popc(bits));
-          int src = 0;
-          if (grp < cnt) {
-            unsigned b = bits;
-            for (int k = 0; k < grp; ++k) b &= b - 1;  // drop the grp lowest set bits
-            src = __ffs(b) - 1;
-          }
-          int tk = __shfl_sync(kFullMask, t, src);
-          const T ak = __shfl_sync(kFullMask, av, src);
-          if (grp >= cnt) tk = -1;
-          // consume the first cnt set bits
-          for (int k = 0; k < cnt; ++k) bits &= bits - 1;
-          // duplicate rows inside the step are applied in entry order, one round each
-          const unsigned peers = __match_any_sync(kFullMask, tk);
+      }
+      unsigned bits = __ballot_sync(kFullMask, t >= 0);
+      while (bits) {
+        const int cnt = min(E, __popc(bits));
+        int src = 0;
+        if (grp < cnt) {
+          unsigned bb = bits;
+          for (int q = 0; q < grp; ++q) bb &= bb - 1;  // drop the grp lowest set bits
+          src = __ffs(bb) - 1;
+        }
+        int tk = __shfl_sync(kFullMask, t, src);
+        const T ak = __shfl_sync(kFullMask, av, src);
+        if (grp >= cnt) tk = -1;
+        for (int q = 0; q < cnt; ++q) bits &= bits - 1;
+        const unsigned peers = __match_any_sync(kFullMask, tk);
+        const bool dup = tk >= 0 && __popc(peers) > Q;
+        if (!__any_sync(kFullMask, dup)) {
+          if (tk >= 0) apply(tile, w, tk, ak, x, col0, colok);
+          __syncwarp();
+        } else {
+          // equal rows inside the step: one round per earlier duplicate, in entry order
           const int rank = __popc(peers & lanemask_lt()) / Q;
-          int rounds = tk >= 0 ? rank : 0;
-#pragma unroll
-          for (int d = 16; d >= 1; d >>= 1) rounds = max(rounds, __shfl_xor_sync(kFullMask, rounds, d));
-          for (int rd = 0; rd <= rounds; ++rd) {
-            if (tk >= 0 && rank == rd) {
-#pragma unroll
-              for (int ci = 0; ci < CI; ++ci) {
-                if (!colok[ci]) continue;
-                V *p = reinterpret_cast<V *>(tile + (int64_t)tk * w + col0[ci]);
-                T cur[VEC];
-                Ops::unpack(*p, cur);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) cur[e] = fma_t(ak, x[ci][e], cur[e]);
-                *p = Ops::pack(cur);
-              }
-            }
+          for (int rd = 0; rd < E; ++rd) {
+            if (tk >= 0 && rank == rd) apply(tile, w, tk, ak, x, col0, colok);
             __syncwarp();
           }
         }
       }
     }
   }
+};
+
+// Block (tile blockIdx.x, group blockIdx.y).  Every consumer warp walks all
+// blocks of the group in order (for its own band of the tile's rows).
+template <typename T, int VEC, int Q, int CI, bool VCS>
+__global__ void __launch_bounds__(kPipeThreads) two_phase_kernel(const TwoPhaseArgs a) {
+  using WP = TwoPhaseWarp<T, VEC, Q, CI, VCS>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Pipe<T, VCS> pipe{smem};
+  T *tile = reinterpret_cast<T *>(smem + PipeLayout<T, VCS>::kExtra);
+
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t t0 = (int64_t)blockIdx.x * a.tile_rows;
+  const int rows = (int)(a.n_t - t0 < a.tile_rows ? a.n_t - t0 : a.tile_rows);
+  const int w = a.w;
+  const int b_lo = a.bounds[blockIdx.y], b_hi = a.bounds[blockIdx.y + 1];
+  for (int q = threadIdx.x; q < rows * w; q += kPipeThreads) tile[q] = T(0);
+  pipe.init();  // (its barrier also publishes the zeroed tile)
+  if (wid == kWarpsPerCta) {  // the producer warp
+    pipe.produce(a.st, b_lo, b_hi, 1);
+  } else {
+    const int band = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
+    const int lo = min(rows, wid * band), hi = min(rows, lo + band);
+    const int ql = lane & (Q - 1);
+    int col0[CI];
+    bool colok[CI];
+#pragma unroll
+    for (int ci = 0; ci < CI; ++ci) {
+      col0[ci] = (ci * Q + ql) * VEC;
+      colok[ci] = col0[ci] < w;
+    }
+    const T *__restrict__ X = static_cast<const T *>(a.X);
+    int i = 0;
+    for (int b = b_lo; b < b_hi; ++b, ++i) {
+      if (!pipe.acquire(i, a.st)) break;
+      const Block k = load_block(a.st.blocks, b);
+      const Staged<T, VCS> sv = stage_views<T, VCS>(k, pipe.buf(i % kStages));
+      if (lo < hi) {
+        if (k.type == 0) {
+          for (int s = k.s0; s < k.s1; ++s) {
+            int n0, n1, rlo = 0, rhi = 0;
+            if (VCS) {
+              rlo = sv.ptr[s];
+              rhi = sv.ptr[s + 1];
+              n0 = sv.vptr[rlo];
+              n1 = sv.vptr[rhi];
+            } else {
+              n0 = sv.ptr[s];
+              n1 = sv.ptr[s + 1];
+            }
+            if (n0 < n1)
+              WP::run(sv, X, a.ldx, tile, w, t0, lo, hi, s, n0, n1, rlo, rhi, col0, colok);
+          }
+        } else {
+          WP::run(sv, X, a.ldx, tile, w, t0, lo, hi, k.s0, k.e0, k.e1, k.r0, k.r1, col0, colok);
+        }
+      }
+      pipe.release(i);
+    }
+  }
   __syncthreads();
-  // write the tile (the final Y when C == 1, else this chunk's partial)
+  if (*pipe.fail()) return;
+  // the tile: final Y when C == 1, else this group's partial
   T *__restrict__ out = static_cast<T *>(a.out) + (int64_t)blockIdx.y * a.part_stride;
-  for (int i = threadIdx.x; i < rows * w; i += kThreads) {
-    const int rr = i / w, c = i - rr * w;
-    out[(t0 + rr) * a.ldo + c] = tile[i];
+  for (int q = threadIdx.x; q < rows * w; q += kPipeThreads) {
+    const int rr = q / w, c = q - rr * w;
+    out[(t0 + rr) * a.ldo + c] = tile[q];
   }
 }
 
-// Y[t, c] = sum over chunks k (in order) of P[k][t, c].
+// Y[t, c] = sum over groups k (in order) of P[k][t, c].
 template <typename T>
 __global__ void combine_kernel(const T *__restrict__ P, int C, int64_t part_stride, int64_t n_t,
                                int w, T *__restrict__ Y, int64_t ldy) {
@@ -321,11 +345,6 @@ inline int pow2ceil(int x) {
   while (p < x) p <<= 1;
   return p;
 }
-
-template <typename T, bool VCS>
-using ScatterPtr = void (*)(const ScatterArgs);
-template <typename T, bool VCS>
-using TwoPhasePtr = void (*)(const TwoPhaseArgs);
 
 struct Shape {
   bool vec;
@@ -397,6 +416,7 @@ struct TwoPhaseK {
 
 template <typename T, bool VCS>
 vs_status atomic_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s) {
+  constexpr int smem = pipe_smem_bytes<T, VCS>(0);
   for (int64_t c0 = 0; c0 < w; c0 += kMaxBlockWidth) {
     const int wb = (int)std::min<int64_t>(kMaxBlockWidth, w - c0);
     const T *xp = static_cast<const T *>(X.p) + c0;
@@ -408,59 +428,54 @@ vs_status atomic_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
       return VS_ERR_UNSUPPORTED;
     }
     ScatterArgs a;
-    a.ptr = m.ptr;
-    a.idx = m.idx;
-    a.vals = m.vals;
-    a.vptr = m.vptr;
+    a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
+                       xp, X.ld, (int)sizeof(T), wb};
     a.X = xp;
     a.ldx = X.ld;
     a.Y = yp;
     a.ldy = Y.ld;
-    a.n_major = (int)m.n_major;
     a.w = wb;
     a.G = std::max(1, std::min(m.g, 32 / sh.Q));
     a.S = 32 / (sh.Q * a.G);
-    a.L = m.L;
-    a.n_chunk_tasks = (int)m.n_chunks;
-    a.tasks = m.chunk_tasks;
-    const int64_t warps = m.n_chunks + (m.n_major + a.S - 1) / a.S;
-    const int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
-    if (blocks > 0) {
-      k<<<(unsigned)blocks, kThreads, 0, s>>>(a);
+    int per_sm = 0;
+    VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kPipeThreads, smem));
+    const int64_t grid = std::min<int64_t>(m.n_blocks, (int64_t)std::max(1, per_sm) * m.n_sm);
+    if (grid > 0) {
+      k<<<(unsigned)grid, kPipeThreads, smem, s>>>(a);
       VS_LAUNCH_CHECK();
     }
   }
   return VS_OK;
 }
 
-constexpr int kTwoPhaseSmem = 200 * 1024;
+constexpr int kTwoPhaseSmem = 224 * 1024;
 
 template <typename T, bool VCS>
 vs_status two_phase_typed(vs_handle_s &h, const Matrix &m, DenseView X, DenseView Y, int64_t w,
                           cudaStream_t s) {
   const int C = m.tp_chunks;
   const int64_t n_t = Y.rows;
+  constexpr int stage = pipe_smem_bytes<T, VCS>(0);
   for (int64_t c0 = 0; c0 < w; c0 += kMaxBlockWidth) {
     const int wb = (int)std::min<int64_t>(kMaxBlockWidth, w - c0);
     const T *xp = static_cast<const T *>(X.p) + c0;
     T *yp = static_cast<T *>(Y.p) + c0;
-    Shape sh = pick_shape<T>(wb, xp, yp, X.ld, C == 1 ? Y.ld : wb);
-    if (C > 1 && sh.vec && wb % (16 / sizeof(T)) != 0) sh.vec = false;
+    Shape sh = pick_shape<T>(wb, xp, xp, X.ld, X.ld);  // Y is written element by element
     auto k = pick_kernel<T, VCS, TwoPhaseK>(sh);
     if (!k) {
       set_error("no two-phase kernel for this width");
       return VS_ERR_UNSUPPORTED;
     }
     const int64_t row_bytes = (int64_t)wb * sizeof(T);
-    const int tile_rows = (int)std::max<int64_t>(1, std::min<int64_t>(n_t, kTwoPhaseSmem / row_bytes));
+    const int tile_rows = (int)std::max<int64_t>(
+        1, std::min<int64_t>(n_t, (kTwoPhaseSmem - stage) / row_bytes));
     const int64_t tiles = (n_t + tile_rows - 1) / tile_rows;
-    const size_t smem = (size_t)tile_rows * row_bytes;
+    const size_t smem = stage + (size_t)tile_rows * row_bytes;
     VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTwoPhaseSmem));
     TwoPhaseArgs a;
-    a.ptr = m.ptr;
-    a.idx = m.idx;
-    a.vals = m.vals;
-    a.vptr = m.vptr;
+    a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
+                       xp, X.ld, (int)sizeof(T), wb};
     a.X = xp;
     a.ldx = X.ld;
     a.bounds = m.tp_bounds;
@@ -472,18 +487,17 @@ vs_status two_phase_typed(vs_handle_s &h, const Matrix &m, DenseView X, DenseVie
       a.ldo = Y.ld;
       a.part_stride = 0;
     } else {
-      const size_t need = (size_t)C * n_t * wb * sizeof(T);
-      VS_TRY(h.tp_partials.reserve(need, s));
+      VS_TRY(h.tp_partials.reserve((size_t)C * n_t * wb * sizeof(T), s));
       a.out = h.tp_partials.p;
       a.ldo = wb;
       a.part_stride = n_t * wb;
     }
     dim3 grid((unsigned)tiles, (unsigned)C);
-    k<<<grid, kThreads, smem, s>>>(a);
+    k<<<grid, kPipeThreads, smem, s>>>(a);
     VS_LAUNCH_CHECK();
     if (C > 1) {
       const int64_t total = n_t * wb;
-      const unsigned blocks = (unsigned)std::min<int64_t>(152 * 8, (total + 255) / 256);
+      const unsigned blocks = (unsigned)std::min<int64_t>((int64_t)m.n_sm * 8, (total + 255) / 256);
       combine_kernel<T><<<std::max(1u, blocks), 256, 0, s>>>(
           static_cast<const T *>(h.tp_partials.p), C, n_t * wb, n_t, wb, yp, Y.ld);
       VS_LAUNCH_CHECK();
@@ -500,12 +514,14 @@ vs_status launch_zero_fill(DenseView Y, int64_t w, size_t dsize, cudaStream_t s)
   const unsigned blocks = (unsigned)std::min<int64_t>(152 * 8, (total + 255) / 256);
   if (Y.ld == w && reinterpret_cast<uintptr_t>(Y.p) % 16 == 0 && (total * dsize) % 16 == 0) {
     const int64_t n16 = total * (int64_t)dsize / 16;
-    zero_fill_vec_kernel<float><<<std::max(1u, std::min<unsigned>(blocks, (unsigned)((n16 + 255) / 256))), 256, 0, s>>>(
-        static_cast<float4 *>(Y.p), n16);
+    zero_fill_vec_kernel<<<std::max(1u, std::min<unsigned>(blocks, (unsigned)((n16 + 255) / 256))),
+                           256, 0, s>>>(static_cast<float4 *>(Y.p), n16);
   } else if (dsize == 8) {
-    zero_fill_kernel<double><<<std::max(1u, blocks), 256, 0, s>>>(static_cast<double *>(Y.p), Y.rows, w, Y.ld);
+    zero_fill_kernel<double><<<std::max(1u, blocks), 256, 0, s>>>(static_cast<double *>(Y.p),
+                                                                    Y.rows, w, Y.ld);
   } else {
-    zero_fill_kernel<float><<<std::max(1u, blocks), 256, 0, s>>>(static_cast<float *>(Y.p), Y.rows, w, Y.ld);
+    zero_fill_kernel<float><<<std::max(1u, blocks), 256, 0, s>>>(static_cast<float *>(Y.p), Y.rows,
+                                                                  w, Y.ld);
   }
   VS_LAUNCH_CHECK();
   return VS_OK;

@@ -1,0 +1,307 @@
+// stage.cuh -- streaming of matrix blocks through shared memory.
+//
+// The stored entries of a matrix are cut (once, at build time, from the matrix
+// alone) into blocks of at most kBlockEntries entries, kBlockRuns runs and
+// kBlockSlices slices.  A block is either
+//   * a slice block: consecutive slices [s0, s1), each short enough for one
+//     warp, or
+//   * a chunk block: chunk k, entries [e0, e1), of a long slice s0; the chunk
+//     is further cut into shares of kShareEntries entries.
+//
+// Each CTA runs a producer/consumer pipeline over its blocks.  One producer
+// warp brings a block's index, value, slice-pointer and run arrays into one of
+// kStages shared-memory buffers with bulk copies (cp.async.bulk), signalled on
+// the buffer's "full" mbarrier; the kWarpsPerCta consumer warps take work
+// units of the block (groups of slices, or shares) from a per-buffer counter
+// and, when the block has no work left, arrive on its "empty" mbarrier, which
+// lets the producer refill the buffer.  Warps never wait for one another
+// except through these barriers, and every wait is bounded in time.
+#pragma once
+
+#include "device_utils.cuh"
+#include "vs_internal.h"
+
+namespace vs {
+
+constexpr int kStages = 4;
+constexpr int kConsumerThreads = kWarpsPerCta * 32;
+constexpr int kPipeThreads = kConsumerThreads + 32;  // plus the producer warp
+constexpr uint64_t kWaitLimitNs = 1000000000ull;     // 1 s
+
+// Element capacity of each staged array, with room for 16-byte alignment slack.
+constexpr int kCapEntries = kBlockEntries + 8;
+constexpr int kCapSlices = kBlockSlices + 8;
+constexpr int kCapRuns = kBlockRuns + 8;
+
+struct StageArrays {
+  const int32_t *ptr;   // slice pointer (CSR entry starts / VCS run starts), padded
+  const int32_t *idx;   // minor indices, padded
+  const void *vals;     // CSR: entry values of T; VCS: run values (float), padded
+  const int32_t *vptr;  // VCS: run entry starts, padded
+  const int4 *blocks;   // [n_blocks][3]
+  int n_blocks;
+  int *err;             // set to 1 when a bounded wait gives up
+  // Optional L2 prefetch of the dense rows X[s0:s1) of each slice block
+  // (misaligned products read X by slice): base, row stride, element size,
+  // valid elements per row; nullptr disables it.
+  const void *xrows;
+  int64_t xld;
+  int xes, xw;
+};
+
+// Byte layout of one stage buffer for value type T.
+template <typename T, bool VCS>
+struct StageLayout {
+  static constexpr int kIdx = 0;
+  static constexpr int kVals = kIdx + kCapEntries * 4;                              // CSR only
+  static constexpr int kPtr = kVals + (VCS ? 0 : kCapEntries * (int)sizeof(T));
+  static constexpr int kVptr = kPtr + kCapSlices * 4;                               // VCS only
+  static constexpr int kRvals = kVptr + (VCS ? kCapRuns * 4 : 0);                   // VCS only
+  static constexpr int kEvals = kRvals + (VCS ? kCapRuns * 4 : 0);                  // VCS only
+  static constexpr int kBytes = kEvals + (VCS ? kCapEntries * 4 : 0);
+  static_assert(kVals % 16 == 0 && kPtr % 16 == 0 && kVptr % 16 == 0 && kRvals % 16 == 0 &&
+                    kEvals % 16 == 0 && kBytes % 16 == 0,
+                "stage arrays must start on 16-byte boundaries");
+};
+
+// Shared memory of a pipelined kernel: the stage buffers, then the control
+// words (full and empty barriers, work counters, failure flag), then `extra`.
+template <typename T, bool VCS>
+struct PipeLayout {
+  static constexpr int kBufs = 0;
+  static constexpr int kFull = kStages * StageLayout<T, VCS>::kBytes;
+  static constexpr int kEmpty = kFull + 8 * kStages;
+  static constexpr int kCounter = kEmpty + 8 * kStages;
+  static constexpr int kFail = kCounter + 4 * kStages;
+  static constexpr int kExtra = (kFail + 4 + 127) / 128 * 128;
+};
+
+template <typename T, bool VCS>
+constexpr int pipe_smem_bytes(int extra) {
+  return PipeLayout<T, VCS>::kExtra + extra;
+}
+
+// A block's descriptor, decoded.
+struct Block {
+  int s0, s1, e0, e1;     // slice range, or (slice, chunk index); entry range
+  int r0, r1, type, lid;  // run range (VCS); 0 = slices, 1 = chunk; long-slice id
+  int first;              // chunk blocks: global index of this chunk's first share
+  int sfirst, nsh;        // chunk blocks: first share of the slice, shares of the slice
+};
+
+__device__ __forceinline__ Block load_block(const int4 *blocks, int b) {
+  const int4 x = blocks[3 * b], y = blocks[3 * b + 1], z = blocks[3 * b + 2];
+  return Block{x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w, z.x, z.y, z.z};
+}
+
+// Work units of a block: groups of S slices, or shares of a chunk.
+__device__ __forceinline__ int block_units(const Block &k, int S) {
+  return k.type == 0 ? (k.s1 - k.s0 + S - 1) / S
+                     : (k.e1 - k.e0 + kShareEntries - 1) / kShareEntries;
+}
+
+// Views of the staged arrays of one block, indexed by global positions.
+template <typename T, bool VCS>
+struct Staged {
+  const int32_t *idx;   // idx[n] for n in [e0, e1)
+  const T *vals;        // vals[n]: CSR the stored values, VCS the run values expanded on chip
+  const int32_t *ptr;   // ptr[s] for s in [s0, s1]
+  const int32_t *vptr;  // VCS: vptr[r] for r in [r0, r1]
+  const float *rvals;   // VCS: rvals[r] for r in [r0, r1)
+};
+
+template <int E>
+__device__ __forceinline__ int align_down(int x) {
+  return x & ~(E - 1);
+}
+template <int E>
+__device__ __forceinline__ int align_up(int x) {
+  return (x + E - 1) & ~(E - 1);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Producer: issue the bulk copies of block `b` into `buf` and arm `bar`.
+template <typename T, bool VCS>
+__device__ __forceinline__ void stage_issue(const StageArrays &a, int b, unsigned char *buf,
+                                            uint64_t *bar) {
+  using LY = StageLayout<T, VCS>;
+  constexpr int VPE = 16 / (int)sizeof(T);  // values per 16 bytes
+  const Block k = load_block(a.blocks, b);
+  uint32_t bytes = 0;
+  int n_idx = 0, n_val = 0, n_ptr = 0, n_vp = 0, n_rv = 0;
+  const int ei = align_down<4>(k.e0);
+  if (k.e1 > k.e0) {
+    n_idx = align_up<4>(k.e1) - ei;
+    bytes += n_idx * 4;
+    if (!VCS) {
+      n_val = align_up<VPE>(k.e1) - align_down<VPE>(k.e0);
+      bytes += n_val * (int)sizeof(T);
+    }
+  }
+  const int pi = align_down<4>(k.s0);
+  if (k.type == 0) {
+    n_ptr = align_up<4>(k.s1 + 1) - pi;
+    bytes += n_ptr * 4;
+  }
+  const int ri = align_down<4>(k.r0);
+  if (VCS) {  // run starts [r0, r1] always (empty slices read vptr[r0]); values [r0, r1)
+    n_vp = align_up<4>(k.r1 + 1) - ri;
+    n_rv = k.r1 > k.r0 ? align_up<4>(k.r1) - ri : 0;
+    bytes += (n_vp + n_rv) * 4;
+  }
+  mbar_arrive_expect_tx(bar, bytes);
+  if (n_idx) bulk_load(buf + LY::kIdx, a.idx + ei, n_idx * 4, bar);
+  if (!VCS && n_val)
+    bulk_load(buf + LY::kVals, static_cast<const T *>(a.vals) + align_down<VPE>(k.e0),
+              n_val * (int)sizeof(T), bar);
+  if (n_ptr) bulk_load(buf + LY::kPtr, a.ptr + pi, n_ptr * 4, bar);
+  if (VCS && n_vp) bulk_load(buf + LY::kVptr, a.vptr + ri, n_vp * 4, bar);
+  if (VCS && n_rv)
+    bulk_load(buf + LY::kRvals, static_cast<const float *>(a.vals) + ri, n_rv * 4, bar);
+  if (a.xrows) {  // dense rows of the block's slices, into L2 (a hint; stays inside the rows)
+    const int s_lo = k.s0, s_hi = k.type == 0 ? k.s1 : k.s0 + 1;
+    const char *base = static_cast<const char *>(a.xrows);
+    uintptr_t lo = reinterpret_cast<uintptr_t>(base + (int64_t)s_lo * a.xld * a.xes);
+    uintptr_t hi =
+        reinterpret_cast<uintptr_t>(base + ((int64_t)(s_hi - 1) * a.xld + a.xw) * a.xes);
+    lo = (lo + 15) & ~uintptr_t(15);
+    hi &= ~uintptr_t(15);
+    if (s_hi > s_lo && hi > lo)
+      prefetch_l2(reinterpret_cast<const void *>(lo), (uint32_t)(hi - lo));
+  }
+}
+
+template <typename T, bool VCS>
+__device__ __forceinline__ Staged<T, VCS> stage_views(const Block &k, unsigned char *buf) {
+  using LY = StageLayout<T, VCS>;
+  constexpr int VPE = 16 / (int)sizeof(T);
+  Staged<T, VCS> v;
+  v.idx = reinterpret_cast<const int32_t *>(buf + LY::kIdx) - align_down<4>(k.e0);
+  v.vals = VCS ? reinterpret_cast<const T *>(buf + LY::kEvals) - align_down<4>(k.e0)
+               : reinterpret_cast<const T *>(buf + LY::kVals) - align_down<VPE>(k.e0);
+  v.ptr = reinterpret_cast<const int32_t *>(buf + LY::kPtr) - align_down<4>(k.s0);
+  v.vptr =
+      VCS ? reinterpret_cast<const int32_t *>(buf + LY::kVptr) - align_down<4>(k.r0) : nullptr;
+  v.rvals =
+      VCS ? reinterpret_cast<const float *>(buf + LY::kRvals) - align_down<4>(k.r0) : nullptr;
+  return v;
+}
+
+// VCS, one consumer warp: writes the run value of each entry n in [n0, n1)
+// into the stage buffer's per-entry value array (entries of different slices
+// or shares never overlap, so warps never write the same word).  Runs
+// [rlo, rhi) cover [n0, n1); one lane per entry, binary search over the runs.
+template <typename T, bool VCS>
+__device__ __forceinline__ void expand_runs(const Block &k, unsigned char *buf, int n0, int n1,
+                                            int rlo, int rhi) {
+  if (!VCS) return;
+  using LY = StageLayout<T, VCS>;
+  const int32_t *vp = reinterpret_cast<const int32_t *>(buf + LY::kVptr) - align_down<4>(k.r0);
+  const float *rv = reinterpret_cast<const float *>(buf + LY::kRvals) - align_down<4>(k.r0);
+  float *ev = reinterpret_cast<float *>(buf + LY::kEvals) - align_down<4>(k.e0);
+  for (int n = n0 + (int)(threadIdx.x & 31); n < n1; n += 32) {
+    int lo = rlo, hi = rhi - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (vp[mid] <= n) lo = mid;
+      else hi = mid - 1;
+    }
+    ev[n] = rv[lo];
+  }
+  __syncwarp();
+}
+
+// The pipeline's shared-memory control words.
+template <typename T, bool VCS>
+struct Pipe {
+  using PL = PipeLayout<T, VCS>;
+  unsigned char *smem;
+  __device__ __forceinline__ unsigned char *buf(int s) const {
+    return smem + PL::kBufs + s * StageLayout<T, VCS>::kBytes;
+  }
+  __device__ __forceinline__ uint64_t *full(int s) const {
+    return reinterpret_cast<uint64_t *>(smem + PL::kFull) + s;
+  }
+  __device__ __forceinline__ uint64_t *empty(int s) const {
+    return reinterpret_cast<uint64_t *>(smem + PL::kEmpty) + s;
+  }
+  __device__ __forceinline__ int *counter(int s) const {
+    return reinterpret_cast<int *>(smem + PL::kCounter) + s;
+  }
+  __device__ __forceinline__ int *fail() const { return reinterpret_cast<int *>(smem + PL::kFail); }
+
+  // All threads; contains __syncthreads.
+  __device__ __forceinline__ void init() const {
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(full(s), 1);
+        mbar_init(empty(s), kWarpsPerCta);
+      }
+      *fail() = 0;
+      fence_barrier_init();
+    }
+    __syncthreads();
+  }
+
+  __device__ __forceinline__ void give_up(const StageArrays &a) const {
+    if ((threadIdx.x & 31) == 0) {
+      atomicOr(fail(), 1);
+      atomicOr(a.err, 1);
+    }
+  }
+
+  // Producer warp (all lanes; lane 0 issues): fills the ring with blocks
+  // b_begin, b_begin + step, ... < b_end, each after the consumers released
+  // its buffer.  Before returning, waits (bounded) until every issued copy has
+  // landed.
+  __device__ __forceinline__ void produce(const StageArrays &a, int b_begin, int b_end,
+                                          int step) const {
+    const int lane = threadIdx.x & 31;
+    int i = 0;
+    for (int b = b_begin; b < b_end; b += step, ++i) {
+      const int s = i % kStages;
+      if (i >= kStages && !mbar_wait_bounded(empty(s), ((i / kStages) - 1) & 1, kWaitLimitNs)) {
+        give_up(a);
+        break;
+      }
+      if (*reinterpret_cast<volatile int *>(fail())) break;
+      if (lane == 0) {
+        *counter(s) = 0;
+        stage_issue<T, VCS>(a, b, buf(s), full(s));
+      }
+      __syncwarp();
+    }
+    if (lane == 0)
+      for (int j = i - kStages < 0 ? 0 : i - kStages; j < i; ++j)
+        mbar_wait_bounded(full(j % kStages), (j / kStages) & 1, kWaitLimitNs);
+  }
+
+  // Consumer warp: waits for the i-th block of this CTA; false if the wait gave up.
+  __device__ __forceinline__ bool acquire(int i, const StageArrays &a) const {
+    if (mbar_wait_bounded(full(i % kStages), (i / kStages) & 1, kWaitLimitNs)) return true;
+    give_up(a);
+    return false;
+  }
+
+  // Consumer warp: done with the i-th block.
+  __device__ __forceinline__ void release(int i) const {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty(i % kStages));
+  }
+
+  // Consumer warp: next work unit of the i-th block (warp-uniform).
+  __device__ __forceinline__ int grab(int i) const {
+    int u = 0;
+    if ((threadIdx.x & 31) == 0) u = atomicAdd(counter(i % kStages), 1);
+    return __shfl_sync(kFullMask, u, 0);
+  }
+};
+
+}  // namespace vs

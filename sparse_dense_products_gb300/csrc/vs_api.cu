@@ -48,18 +48,18 @@ int64_t Matrix::layout_bytes() const {
 }
 
 int64_t Matrix::meta_bytes() const {
-  return (int64_t)sizeof(int4) * n_chunks + (int64_t)sizeof(int) * n_long +
-         (int64_t)dsize() * kMaxBlockWidth * n_chunks + (int64_t)sizeof(int32_t) * (tp_chunks + 1);
+  return (int64_t)sizeof(int4) * 3 * n_blocks + (int64_t)sizeof(int) * (n_long + 1) +
+         (int64_t)dsize() * kMaxBlockWidth * n_shares + (int64_t)sizeof(int32_t) * (tp_chunks + 1);
 }
 
 void free_matrix(Matrix &m) {
-  for (void *p : {(void *)m.ptr, (void *)m.idx, m.vals, (void *)m.vptr, (void *)m.chunk_tasks,
-                  (void *)m.counters, m.partials, (void *)m.tp_bounds})
+  for (void *p : {(void *)m.ptr, (void *)m.idx, m.vals, (void *)m.vptr, (void *)m.blocks,
+                  (void *)m.counters, m.partials, (void *)m.tp_bounds, (void *)m.err})
     if (p) cudaFree(p);
   m.ptr = m.idx = m.vptr = m.tp_bounds = nullptr;
   m.vals = m.partials = nullptr;
-  m.chunk_tasks = nullptr;
-  m.counters = nullptr;
+  m.blocks = nullptr;
+  m.counters = m.err = nullptr;
 }
 
 vs_status Scratch::reserve(size_t need, cudaStream_t s) {
@@ -298,9 +298,10 @@ vs_status vs_info(vs_handle A, vs_info_t *info) {
   info->n_cols = m.n_cols;
   info->nnz = m.nnz;
   info->n_runs = m.R;
-  info->chunk_len = m.L;
+  info->chunk_len = kBlockEntries;
   info->n_long_slices = m.n_long;
   info->n_chunks = m.n_chunks;
+  info->n_blocks = m.n_blocks;
   info->has_transpose = A->T != nullptr;
   return VS_OK;
 }

@@ -47,10 +47,16 @@ int64_t launch_count();
 
 // ------------------------------------------------------------------ layout
 
-// Chunk length L: slices longer than L entries are split into chunks of L
-// entries, combined in chunk order.  A constant, so the summation order of a
-// product depends on the matrix only.
-constexpr int kChunkLen = 1024;
+// Matrix blocks streamed through shared memory (stage.cuh): at most this many
+// entries, runs and slices per block.  A slice with more entries (or, in VCS,
+// more runs) is "long": it is cut into chunks within the same limits, and each
+// chunk into shares of kShareEntries entries.  The cut points depend on the
+// matrix only, so the summation order does too.
+constexpr int kBlockEntries = 1024;
+constexpr int kBlockRuns = 256;
+constexpr int kBlockSlices = 256;
+constexpr int kShareEntries = 256;
+constexpr int kWarpsPerCta = 8;   // consumer warps; one more warp produces
 
 // Widest column block one kernel launch handles; wider products loop.
 constexpr int kMaxBlockWidth = 64;
@@ -72,17 +78,21 @@ struct Matrix {
 
   // Matrix-only kernel parameters.
   int g = 1;                    // group size: threads per slice (power of 2 in [1, 32])
-  int L = kChunkLen;            // chunk length
-  int64_t n_long = 0;           // slices longer than L
+  int64_t n_blocks = 0;         // staged blocks
+  int4 *blocks = nullptr;       // [n_blocks][3] descriptors (stage.cuh)
+  int64_t n_long = 0;           // long slices
   int64_t n_chunks = 0;         // chunks over all long slices
-  int4 *chunk_tasks = nullptr;  // [n_chunks] {slice, chunk k, long id, first partial}
+  int64_t n_shares = 0;         // shares over all long slices
   int *counters = nullptr;      // [n_long] arrival counters (always left at 0)
-  void *partials = nullptr;     // [n_chunks * kMaxBlockWidth] of dtype
+  void *partials = nullptr;     // [n_shares * kMaxBlockWidth] of dtype
+  int *err = nullptr;           // device flag: a bounded wait gave up
   bool sorted_segments = false; // minor indices ascend inside every run / row
+  int n_sm = 1;                 // multiprocessors of the device the matrix lives on
 
-  // Two-phase (deterministic misaligned) chunking of the slices: matrix-only.
+  // Two-phase (deterministic misaligned) chunking: C groups of consecutive
+  // blocks with balanced entry counts, fixed by the matrix.
   int tp_chunks = 0;                // C
-  int32_t *tp_bounds = nullptr;     // [C+1] slice boundaries, balanced by entries
+  int32_t *tp_bounds = nullptr;     // [C+1] block boundaries of the groups
 
   size_t dsize() const { return dtype == VS_F64 ? 8 : 4; }
   int64_t layout_bytes() const;

@@ -190,6 +190,8 @@ def test_degenerate_shapes(shape, nnz, layout, major, direction):
         for variant in _variants(major, direction):
             out = vs.empty_out(A, w, direction)
             out.fill_(float("nan"))  # every element must be written
+            if variant == "transposed":
+                A.attach_transpose()
             vs.spmm(A, B, direction, variant, out=out)
             torch.cuda.synchronize()
             got = gpu_out_rows(out, direction)
