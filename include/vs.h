@@ -181,6 +181,34 @@ vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direct
                   vs_variant variant, cudaStream_t stream);
 
 /*
+ * vs_spmm_noalloc -- the deterministic product of vs_spmm (VS_DETERMINISTIC)
+ * for callers that must not allocate device memory when they run a product:
+ * code running inside stream capture, code whose device memory comes from a
+ * pool or allocator it does not control, or code that may not call cudaMalloc
+ * at that point.  It calls no cudaMalloc, cudaFree or allocating library
+ * routine.  (The pages have no counterpart: this entry point exists for such
+ * callers only.)
+ *
+ * Arguments, layouts and results as for vs_spmm with VS_DETERMINISTIC: aligned
+ * directions run the same gather (which needs no scratch beyond what the
+ * handle got at build time), misaligned directions the same two-phase scheme,
+ * with its per-group partial sums in a fixed 32 MiB device array that the
+ * library declares statically -- every GPU that loads the library holds those
+ * 32 MiB until the process exits.  Results are bit-identical to vs_spmm's.
+ * The column block is narrowed until the partial sums fit; a product whose
+ * partials do not fit even one column returns VS_ERR_UNSUPPORTED with the
+ * sizes in vs_last_error().
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array, which keeps whatever the last call
+ * left in it; calls whose work overlaps on the GPU (other streams, other
+ * threads) race on it and must be serialised by the caller.
+ */
+vs_status vs_spmm_noalloc(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direction dir,
+                          cudaStream_t stream);
+
+/*
  * vs_spmm_host -- vs_spmm with B and out in HOST memory (pinned memory is
  * fastest).  Copies B to device staging owned by the handle, runs vs_spmm on
  * `stream`, copies the result back and synchronises `stream` before

@@ -21,6 +21,8 @@
 //    adds the C group partials of every element in group order.  The order of
 //    every element's sum therefore depends on the matrix alone.
 #include <algorithm>
+#include <mutex>
+#include <string>
 
 #include "stage.cuh"
 
@@ -506,7 +508,122 @@ vs_status two_phase_typed(vs_handle_s &h, const Matrix &m, DenseView X, DenseVie
   return VS_OK;
 }
 
+// ------------------------------------------------------------------ allocation-free variant
+
+// Scratch for callers that cannot allocate device memory at call time (code
+// running inside stream capture, under a memory pool they do not own, or in a
+// process whose allocator is reserved for something else): the group partials
+// of the two-phase scheme live in this fixed array instead of handle scratch.
+// Every GPU that loads the library holds it until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_addr[kMaxDevices] = {};
+
+// The device address of g_static_scratch on the current device, looked up once
+// per device (the host-side name is only a stand-in for it).
+vs_status static_scratch_address(void **out) {
+  int dev = 0;
+  VS_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device ordinal beyond the static scratch table");
+    return VS_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void *p = nullptr;
+    VS_CUDA(cudaGetSymbolAddress(&p, g_static_scratch));
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return VS_OK;
+}
+
+// The two-phase product with its group partials in g_static_scratch.  The
+// column block is narrowed until the partials fit; the order of every
+// element's sum does not depend on the column block, so the bits match the
+// handle-scratch path.
+template <typename T, bool VCS>
+vs_status two_phase_static_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w,
+                                 cudaStream_t s) {
+  const int C = m.tp_chunks;
+  const int64_t n_t = Y.rows;
+  constexpr int stage = pipe_smem_bytes<T, VCS>(0);
+  constexpr int VW = 16 / sizeof(T);
+  void *scratch = nullptr;
+  int64_t wmax = kMaxBlockWidth;
+  if (C > 1) {
+    VS_TRY(static_scratch_address(&scratch));
+    const int64_t per_col = (int64_t)C * n_t * (int64_t)sizeof(T);
+    wmax = std::min<int64_t>(kMaxBlockWidth, (int64_t)kStaticScratchBytes / std::max<int64_t>(per_col, 1));
+    if (wmax >= VW) wmax = wmax / VW * VW;
+    if (wmax < 1) {
+      set_error("vs_spmm_noalloc: the partial sums need " + std::to_string(per_col) +
+                " bytes per column; the static scratch holds " +
+                std::to_string(kStaticScratchBytes) + " bytes");
+      return VS_ERR_UNSUPPORTED;
+    }
+  }
+  for (int64_t c0 = 0; c0 < w; c0 += wmax) {
+    const int wb = (int)std::min<int64_t>(wmax, w - c0);
+    const T *xp = static_cast<const T *>(X.p) + c0;
+    T *yp = static_cast<T *>(Y.p) + c0;
+    Shape sh = pick_shape<T>(wb, xp, xp, X.ld, X.ld);
+    auto k = pick_kernel<T, VCS, TwoPhaseK>(sh);
+    if (!k) {
+      set_error("no two-phase kernel for this width");
+      return VS_ERR_UNSUPPORTED;
+    }
+    const int64_t row_bytes = (int64_t)wb * sizeof(T);
+    const int tile_rows = (int)std::max<int64_t>(
+        1, std::min<int64_t>(n_t, (kTwoPhaseSmem - stage) / row_bytes));
+    const int64_t tiles = (n_t + tile_rows - 1) / tile_rows;
+    const size_t smem = stage + (size_t)tile_rows * row_bytes;
+    VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTwoPhaseSmem));
+    TwoPhaseArgs a;
+    a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
+                       xp, X.ld, (int)sizeof(T), wb};
+    a.X = xp;
+    a.ldx = X.ld;
+    a.bounds = m.tp_bounds;
+    a.n_t = n_t;
+    a.tile_rows = tile_rows;
+    a.w = wb;
+    if (C == 1) {
+      a.out = yp;
+      a.ldo = Y.ld;
+      a.part_stride = 0;
+    } else {
+      a.out = scratch;
+      a.ldo = wb;
+      a.part_stride = n_t * wb;
+    }
+    dim3 grid((unsigned)tiles, (unsigned)C);
+    k<<<grid, kPipeThreads, smem, s>>>(a);
+    VS_LAUNCH_CHECK();
+    if (C > 1) {
+      const int64_t total = n_t * wb;
+      const unsigned blocks = (unsigned)std::min<int64_t>((int64_t)m.n_sm * 8, (total + 255) / 256);
+      combine_kernel<T><<<std::max(1u, blocks), 256, 0, s>>>(static_cast<const T *>(scratch), C,
+                                                             n_t * wb, n_t, wb, yp, Y.ld);
+      VS_LAUNCH_CHECK();
+    }
+  }
+  return VS_OK;
+}
+
 }  // namespace
+
+vs_status launch_scatter_two_phase_static(const Matrix &m, DenseView X, DenseView Y, int64_t w,
+                                          cudaStream_t s) {
+  if (w <= 0 || Y.rows == 0) return VS_OK;
+  if (m.n_major == 0 || m.nnz == 0) return launch_zero_fill(Y, w, m.dsize(), s);
+  if (m.layout == VS_LAYOUT_VCS) return two_phase_static_typed<float, true>(m, X, Y, w, s);
+  if (m.dtype == VS_F64) return two_phase_static_typed<double, false>(m, X, Y, w, s);
+  return two_phase_static_typed<float, false>(m, X, Y, w, s);
+}
 
 vs_status launch_zero_fill(DenseView Y, int64_t w, size_t dsize, cudaStream_t s) {
   if (w <= 0 || Y.rows <= 0) return VS_OK;

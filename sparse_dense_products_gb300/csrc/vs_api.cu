@@ -233,6 +233,19 @@ vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direct
   }
 }
 
+vs_status vs_spmm_noalloc(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direction dir,
+                          cudaStream_t stream) {
+  if (!valid_handle(A)) return invalid("NULL handle");
+  if (!B || !out) return invalid("NULL operand descriptor");
+  DenseView X, Y;
+  int64_t w = 0;
+  bool aligned = false;
+  VS_TRY(frame(A->A, *B, *out, dir, X, Y, w, aligned));
+  if (w == 0 || Y.rows == 0) return VS_OK;
+  if (aligned) return launch_gather(A->A, X, Y, w, stream);
+  return launch_scatter_two_phase_static(A->A, X, Y, w, stream);
+}
+
 vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_host,
                        vs_direction dir, vs_variant variant, cudaStream_t stream) {
   if (!valid_handle(A)) return invalid("NULL handle");

@@ -159,6 +159,11 @@ vs_status launch_scatter_atomic(const Matrix &m, DenseView X, DenseView Y, int64
 vs_status launch_scatter_two_phase(vs_handle_s &h, const Matrix &m, DenseView X, DenseView Y,
                                    int64_t w, cudaStream_t s);
 
+// The same two-phase product with its partial sums in a statically allocated
+// device array (no allocation at call time).
+vs_status launch_scatter_two_phase_static(const Matrix &m, DenseView X, DenseView Y, int64_t w,
+                                          cudaStream_t s);
+
 // Y[0:rows, 0:w] = 0 with row stride ld.
 vs_status launch_zero_fill(DenseView Y, int64_t w, size_t dsize, cudaStream_t s);
 
