@@ -1,0 +1,9 @@
+// gather_f64_csr.cu -- instantiates the aligned gather (gather_impl.cuh) for
+// double values, CSR layout.
+#include "gather_impl.cuh"
+
+namespace vs {
+vs_status launch_gather_f64_csr(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s) {
+  return gather_detail::launch_typed<double, false>(m, X, Y, w, s);
+}
+}  // namespace vs

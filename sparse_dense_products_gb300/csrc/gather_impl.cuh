@@ -1,0 +1,326 @@
+// gather_impl.cuh -- the aligned direction: Y[s, :] = sum over the entries
+// (t, a) of major slice s of a * X[t, :].  Covers CSR@B, VCSR@B, B@VCSC and
+// B@CSC (every aligned product maps onto this slice frame, see vs_api.cu), and
+// the misaligned products that run over an attached exact transpose.
+// Instantiated per value type and layout by gather_f32_csr.cu,
+// gather_f32_vcs.cu and gather_f64_csr.cu.
+//
+// "Add CUDA transfer and matmul kernels for the normalized views", "The
+// kernels": one warp per major slice, lanes split between the dense width and
+// the slice's nonzeros so narrow widths leave no lanes idle; aligned
+// directions accumulate in registers and reduce with shuffles.
+// "Regridder", "How it is built": each slice gets a group of g threads, g set
+// by the matrix alone (the mean entries per slice rounded down to a power of
+// two, capped at a warp), summed in a fixed tree, so a product repeats exactly
+// and a column gives the same numbers alone or in a batch.
+//
+// Summation order of one output element (s, c), fixed by the matrix alone:
+//   * a run of entries (a whole short slice, or one share of a long slice) is
+//     summed as g logical partials -- partial k takes the entries n with
+//     (n - start) mod g == k, with fused multiply-adds in entry order -- which
+//     meet in the butterfly p[k] += p[k + h], h = g/2, ..., 1;
+//   * a long slice is cut into chunks (at most kBlockEntries entries and
+//     kBlockRuns runs, cut points fixed by the matrix) and every chunk into
+//     shares of kShareEntries entries; the share results are added in share
+//     order ((p0 + p1) + p2) + ... by the last share of the slice to finish.
+// Physically G slots of a slice each hold NP = g / G partials in registers
+// (Q lanes per slot across a tile of Q * VEC columns; wider products take
+// several column passes over the same staged entries; narrow ones put several
+// slices in one warp).  In-lane adds, then
+// shuffles, reproduce the same tree for every width, so bits never depend on w.
+//
+// Data movement: entries, values, slice pointers and runs arrive in shared
+// memory by bulk copies through a 4-deep ring fed by a producer warp
+// (stage.cuh); the producer warp also expands VCS run values to per-entry
+// values in shared memory; the dense rows X[t, :] are gathered through L1 with
+// 16-byte vector loads.
+#pragma once
+
+#include <algorithm>
+
+#include "stage.cuh"
+
+namespace vs {
+namespace gather_detail {
+
+struct GatherArgs {
+  StageArrays st;
+  const void *X;
+  int64_t ldx;
+  void *Y;
+  int64_t ldy;
+  int w;           // columns in this launch (<= kMaxBlockWidth)
+  void *partials;  // [n_shares][kMaxBlockWidth] of T
+  int *counters;   // [n_long]
+};
+
+__device__ __forceinline__ int atomic_add_release(int *p, int v) {
+  int old;
+  asm volatile("atom.add.release.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Sums entries [n0, n1) of one slice for the column tile starting at `col`
+// (this lane's VEC columns) and runs the fixed tree; acc[0] holds the result
+// in the slice's slot-0 lanes.
+template <typename T, int VEC, int Q, int G, int NP, bool VCS>
+__device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const T *__restrict__ Xc,
+                                             int64_t ldx, int n0, int n1, int slot, bool cok,
+                                             T (&acc)[NP][VEC]) {
+  using V = typename VecT<T, VEC>::type;
+  using Ops = VecOps<T, VEC>;
+  constexpr int STEP = G * NP;
+#pragma unroll
+  for (int i = 0; i < NP; ++i)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[i][e] = T(0);
+  const int nfull = (n1 - n0) / STEP;
+  int n = n0 + slot;
+  int it = 0;
+  // two steps at a time: 2 NP independent loads in flight per lane
+  for (; it + 1 < nfull; it += 2, n += 2 * STEP) {
+    int j[2 * NP];
+    T av[2 * NP];
+#pragma unroll
+    for (int i = 0; i < 2 * NP; ++i) {
+      j[i] = sv.idx[n + i * G];
+      av[i] = sv.vals[n + i * G];
+    }
+    V x[2 * NP];
+#pragma unroll
+    for (int i = 0; i < 2 * NP; ++i)
+      x[i] = cok ? ld_gather(reinterpret_cast<const V *>(Xc + (int64_t)j[i] * ldx)) : V{};
+#pragma unroll
+    for (int i = 0; i < 2 * NP; ++i) {  // step it, then step it + 1, partial by partial
+      T xe[VEC];
+      Ops::unpack(x[i], xe);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[i % NP][e] = fma(av[i], xe[e], acc[i % NP][e]);
+    }
+  }
+  for (; it < nfull; ++it, n += STEP) {
+    int j[NP];
+    T av[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      j[i] = sv.idx[n + i * G];
+      av[i] = sv.vals[n + i * G];
+    }
+    V x[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i)
+      x[i] = cok ? ld_gather(reinterpret_cast<const V *>(Xc + (int64_t)j[i] * ldx)) : V{};
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      T xe[VEC];
+      Ops::unpack(x[i], xe);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[i][e] = fma(av[i], xe[e], acc[i][e]);
+    }
+  }
+  // the last, partial step
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const int nn = n + i * G;
+    if (nn < n1) {
+      const int jj = sv.idx[nn];
+      const T a = sv.vals[nn];
+      const V x = cok ? ld_gather(reinterpret_cast<const V *>(Xc + (int64_t)jj * ldx)) : V{};
+      T xe[VEC];
+      Ops::unpack(x, xe);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[i][e] = fma(a, xe[e], acc[i][e]);
+    }
+  }
+  // the fixed tree: in-lane levels (strides h*G), then across slots (strides < G)
+#pragma unroll
+  for (int h = NP / 2; h >= 1; h >>= 1)
+#pragma unroll
+    for (int i = 0; i < h; ++i)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[i][e] = acc[i][e] + acc[i + h][e];
+#pragma unroll
+  for (int sft = G / 2; sft >= 1; sft >>= 1)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e)
+      acc[0][e] = acc[0][e] + __shfl_xor_sync(kFullMask, acc[0][e], sft * Q);
+}
+
+#ifndef VS_GATHER_MIN_CTAS
+#define VS_GATHER_MIN_CTAS 3
+#endif
+template <typename T, int VEC, int Q, int G, int NP, bool VCS>
+__global__ void __launch_bounds__(kPipeThreads, VS_GATHER_MIN_CTAS) gather_kernel(const GatherArgs a) {
+  using V = typename VecT<T, VEC>::type;
+  using Ops = VecOps<T, VEC>;
+  constexpr int S = 32 / (Q * G);  // slices per warp work unit
+  constexpr int TW = Q * VEC;      // columns per pass
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Pipe<T, VCS> pipe{smem};
+  pipe.init();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (wid == kWarpsPerCta) {  // the producer warp
+    pipe.produce(a.st, blockIdx.x, a.st.n_blocks, gridDim.x);
+    return;
+  }
+  const int ql = lane % Q;
+  const int slot = (lane / Q) % G;
+  const int sub = lane / (Q * G);
+  const T *__restrict__ X = static_cast<const T *>(a.X);
+  T *__restrict__ Y = static_cast<T *>(a.Y);
+  T *__restrict__ P = static_cast<T *>(a.partials);
+  const int w = a.w;
+
+  int i = 0, rot = 0;  // rot: units handed out so far, mod kWarpsPerCta
+  for (int b = blockIdx.x; b < a.st.n_blocks; b += gridDim.x, ++i) {
+    if (!pipe.acquire(i, a.st)) return;
+    const Block k = load_block(a.st.blocks, b);
+    unsigned char *buf = pipe.buf(i % kStages);
+    const Staged<T, VCS> sv = stage_views<T, VCS>(k, buf);
+    const int units = block_units(k, S);
+    T acc[NP][VEC];
+    // work units go round-robin to the consumer warps, continuing across blocks
+    const int u0 = (wid - rot + kWarpsPerCta) % kWarpsPerCta;
+    rot = (rot + units) % kWarpsPerCta;
+    for (int u = u0; u < units; u += kWarpsPerCta) {
+      if (k.type == 0) {
+        // ---- S consecutive slices, one per sub-group
+        const int sa = k.s0 + u * S;
+        const int s = sa + sub;
+        const bool mine = s < k.s1;
+        int n0 = 0, n1 = 0;
+        if (mine) {
+          n0 = VCS ? sv.vptr[sv.ptr[s]] : sv.ptr[s];
+          n1 = VCS ? sv.vptr[sv.ptr[s + 1]] : sv.ptr[s + 1];
+        }
+        for (int cp = 0; cp < w; cp += TW) {
+          const int col = cp + ql * VEC;
+          const bool cok = col < w;
+          gather_range<T, VEC, Q, G, NP, VCS>(sv, X + col, a.ldx, n0, n1, slot, cok, acc);
+          if (mine && slot == 0 && cok)
+            *reinterpret_cast<V *>(Y + (int64_t)s * a.ldy + col) = Ops::pack(acc[0]);
+        }
+      } else {
+        // ---- share u of a chunk of a long slice: publish its partial; the last
+        // share of the slice to arrive adds all of them in share order
+        const int na = k.e0 + u * kShareEntries, nb = min(k.e1, na + kShareEntries);
+        const int n0 = sub == 0 ? na : 0, n1 = sub == 0 ? nb : 0;
+        for (int cp = 0; cp < w; cp += TW) {
+          const int col = cp + ql * VEC;
+          const bool cok = col < w;
+          gather_range<T, VEC, Q, G, NP, VCS>(sv, X + col, a.ldx, n0, n1, slot, cok, acc);
+          if (sub == 0 && slot == 0 && cok)
+            *reinterpret_cast<V *>(P + (int64_t)(k.first + u) * kMaxBlockWidth + col) =
+                Ops::pack(acc[0]);
+        }
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomic_add_release(a.counters + k.lid, 1) == k.nsh - 1;
+        last = __shfl_sync(kFullMask, last, 0);
+        if (last) {
+          __threadfence();
+          for (int c = lane; c < w; c += 32) {
+            T sum = __ldcg(P + (int64_t)k.sfirst * kMaxBlockWidth + c);
+            for (int q = 1; q < k.nsh; ++q)
+              sum = sum + __ldcg(P + (int64_t)(k.sfirst + q) * kMaxBlockWidth + c);
+            Y[(int64_t)k.s0 * a.ldy + c] = sum;
+          }
+          if (lane == 0) a.counters[k.lid] = 0;  // re-armed for the next launch
+        }
+      }
+    }
+    pipe.release(i);
+  }
+}
+
+// ------------------------------------------------------------------ dispatch
+
+template <typename T, bool VCS>
+using KernelPtr = void (*)(const GatherArgs);
+
+// Slots per slice G = min(g, kMaxSlots); each lane then holds NP = g / G <= 4
+// logical partials, and a warp works on 32 / (Q G) slices at a time.
+#ifndef VS_MAX_SLOTS
+#define VS_MAX_SLOTS 8
+#endif
+constexpr int kMaxSlots = VS_MAX_SLOTS;
+
+template <typename T, int VEC, int Q, int G, bool VCS>
+KernelPtr<T, VCS> pick_np(int np) {
+  if constexpr (G == kMaxSlots || G * Q == 32) {
+    if constexpr (Q * G * 2 <= 64)
+      if (np == 2) return gather_kernel<T, VEC, Q, G, 2, VCS>;
+    if constexpr (Q * G * 4 <= 128)
+      if (np == 4) return gather_kernel<T, VEC, Q, G, 4, VCS>;
+  }
+  return np == 1 ? gather_kernel<T, VEC, Q, G, 1, VCS> : nullptr;
+}
+
+template <typename T, int VEC, int Q, bool VCS>
+KernelPtr<T, VCS> pick_g(int G, int np) {
+  switch (G) {
+    case 1: return pick_np<T, VEC, Q, 1, VCS>(np);
+    case 2: return pick_np<T, VEC, Q, 2, VCS>(np);
+    case 4: return pick_np<T, VEC, Q, 4, VCS>(np);
+    case 8: return pick_np<T, VEC, Q, 8, VCS>(np);
+    case 16: if constexpr (kMaxSlots >= 16 && Q <= 2) return pick_np<T, VEC, Q, 16, VCS>(np); break;
+    case 32: if constexpr (kMaxSlots >= 32 && Q == 1) return pick_np<T, VEC, Q, 32, VCS>(np); break;
+  }
+  return nullptr;
+}
+
+template <typename T, int VEC, bool VCS>
+KernelPtr<T, VCS> pick_q(int Q, int G, int np) {
+  switch (Q) {
+    case 1: return pick_g<T, VEC, 1, VCS>(G, np);
+    case 2: return pick_g<T, VEC, 2, VCS>(G, np);
+    case 4: return pick_g<T, VEC, 4, VCS>(G, np);
+  }
+  return nullptr;
+}
+
+template <typename T, bool VCS>
+vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s) {
+  constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
+  constexpr int smem = pipe_smem_bytes<T, VCS>(0);
+  for (int64_t c0 = 0; c0 < w; c0 += kMaxBlockWidth) {
+    const int wb = (int)std::min<int64_t>(kMaxBlockWidth, w - c0);
+    const T *xp = static_cast<const T *>(X.p) + c0;
+    T *yp = static_cast<T *>(Y.p) + c0;
+    const bool vec = wb % VW == 0 && reinterpret_cast<uintptr_t>(xp) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(yp) % 16 == 0 && X.ld % VW == 0 &&
+                     Y.ld % VW == 0;
+    // lanes per slot across the width: one 16-byte vector (or one element) each, up to 4
+    const int ncol = vec ? wb / VW : wb;
+    const int Q = ncol >= 3 ? 4 : ncol;  // 1, 2 or 4
+    const int G = std::min(std::min(m.g, kMaxSlots), 32 / Q);
+    const int NP = m.g / G;
+    KernelPtr<T, VCS> k = vec ? pick_q<T, VW, VCS>(Q, G, NP) : pick_q<T, 1, VCS>(Q, G, NP);
+    if (!k) {
+      set_error("no gather kernel for this width and group size");
+      return VS_ERR_UNSUPPORTED;
+    }
+    GatherArgs a;
+    a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
+                       nullptr, 0, 0, 0};
+    a.X = xp;
+    a.ldx = X.ld;
+    a.Y = yp;
+    a.ldy = Y.ld;
+    a.w = wb;
+    a.partials = m.partials;
+    a.counters = m.counters;
+    int per_sm = 0;
+    VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kPipeThreads, smem));
+    const int64_t grid = std::min<int64_t>(m.n_blocks, (int64_t)std::max(1, per_sm) * m.n_sm);
+    if (grid > 0) {
+      k<<<(unsigned)grid, kPipeThreads, smem, s>>>(a);
+      VS_LAUNCH_CHECK();
+    }
+  }
+  return VS_OK;
+}
+
+}  // namespace gather_detail
+}  // namespace vs

@@ -92,25 +92,18 @@ __global__ void __launch_bounds__(kPipeThreads) scatter_atomic_kernel(const Scat
     colok[ci] = col0[ci] < a.w;
   }
 
-  int i = 0;
+  int i = 0, rot = 0;  // rot: units handed out so far, mod kWarpsPerCta
   for (int b = blockIdx.x; b < a.st.n_blocks; b += gridDim.x, ++i) {
     if (!pipe.acquire(i, a.st)) return;
     const Block k = load_block(a.st.blocks, b);
     const Staged<T, VCS> sv = stage_views<T, VCS>(k, pipe.buf(i % kStages));
     const int units = block_units(k, a.S);
     T x[CI][VEC];
-    for (int u = pipe.grab(i); u < units; u = pipe.grab(i)) {
+    // work units go round-robin to the consumer warps, continuing across blocks
+    const int u0 = (wid - rot + kWarpsPerCta) % kWarpsPerCta;
+    rot = (rot + units) % kWarpsPerCta;
+    for (int u = u0; u < units; u += kWarpsPerCta) {
       int s, n0 = 0, n1 = 0;
-      if (VCS) {  // run values of this unit's entries, on chip
-        if (k.type == 0) {
-          const int sa = k.s0 + u * a.S, sb = min(k.s1, sa + a.S);
-          expand_runs<T, VCS>(k, pipe.buf(i % kStages), sv.vptr[sv.ptr[sa]], sv.vptr[sv.ptr[sb]],
-                              sv.ptr[sa], sv.ptr[sb]);
-        } else {
-          expand_runs<T, VCS>(k, pipe.buf(i % kStages), k.e0 + u * kShareEntries,
-                              min(k.e1, k.e0 + (u + 1) * kShareEntries), k.r0, k.r1);
-        }
-      }
       if (k.type == 0) {
         s = k.s0 + u * a.S + sub;
         if (s < k.s1) {

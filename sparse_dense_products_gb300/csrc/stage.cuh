@@ -58,9 +58,10 @@ struct StageLayout {
   static constexpr int kVptr = kPtr + kCapSlices * 4;                               // VCS only
   static constexpr int kRvals = kVptr + (VCS ? kCapRuns * 4 : 0);                   // VCS only
   static constexpr int kEvals = kRvals + (VCS ? kCapRuns * 4 : 0);                  // VCS only
-  static constexpr int kBytes = kEvals + (VCS ? kCapEntries * 4 : 0);
+  static constexpr int kBitmap = kEvals + (VCS ? kCapEntries * 4 : 0);              // VCS only
+  static constexpr int kBytes = kBitmap + (VCS ? ((kCapEntries + 31) / 32 * 4 + 15) / 16 * 16 : 0);
   static_assert(kVals % 16 == 0 && kPtr % 16 == 0 && kVptr % 16 == 0 && kRvals % 16 == 0 &&
-                    kEvals % 16 == 0 && kBytes % 16 == 0,
+                    kEvals % 16 == 0 && kBitmap % 16 == 0 && kBytes % 16 == 0,
                 "stage arrays must start on 16-byte boundaries");
 };
 
@@ -71,7 +72,8 @@ struct PipeLayout {
   static constexpr int kBufs = 0;
   static constexpr int kFull = kStages * StageLayout<T, VCS>::kBytes;
   static constexpr int kEmpty = kFull + 8 * kStages;
-  static constexpr int kCounter = kEmpty + 8 * kStages;
+  static constexpr int kReady = kEmpty + 8 * kStages;  // VCS: run values expanded
+  static constexpr int kCounter = kReady + 8 * kStages;
   static constexpr int kFail = kCounter + 4 * kStages;
   static constexpr int kExtra = (kFail + 4 + 127) / 128 * 128;
 };
@@ -232,6 +234,9 @@ struct Pipe {
   __device__ __forceinline__ uint64_t *empty(int s) const {
     return reinterpret_cast<uint64_t *>(smem + PL::kEmpty) + s;
   }
+  __device__ __forceinline__ uint64_t *ready(int s) const {
+    return reinterpret_cast<uint64_t *>(smem + PL::kReady) + s;
+  }
   __device__ __forceinline__ int *counter(int s) const {
     return reinterpret_cast<int *>(smem + PL::kCounter) + s;
   }
@@ -243,6 +248,7 @@ struct Pipe {
       for (int s = 0; s < kStages; ++s) {
         mbar_init(full(s), 1);
         mbar_init(empty(s), kWarpsPerCta);
+        mbar_init(ready(s), 1);
       }
       *fail() = 0;
       fence_barrier_init();
@@ -257,27 +263,85 @@ struct Pipe {
     }
   }
 
+  // VCS, producer warp: once block j (number b) has landed, write the run
+  // value of each of its entries into the per-entry value array and mark the
+  // stage ready.  Run starts go into a bitmap over the block's entries; the
+  // run of entry n is then r0 - 1 + (run starts in [e0, n]), counted with
+  // popcounts 32 entries at a time.
+  __device__ __forceinline__ bool expand(const StageArrays &a, int j, int b) const {
+    using LY = StageLayout<T, VCS>;
+    const int s = j % kStages;
+    if (!mbar_wait_bounded(full(s), (j / kStages) & 1, kWaitLimitNs)) return false;
+    const int lane = threadIdx.x & 31;
+    const Block k = load_block(a.blocks, b);
+    unsigned char *bp = buf(s);
+    const int eb = align_down<4>(k.e0);
+    const int32_t *vp = reinterpret_cast<const int32_t *>(bp + LY::kVptr) - align_down<4>(k.r0);
+    const float *rv = reinterpret_cast<const float *>(bp + LY::kRvals) - align_down<4>(k.r0);
+    float *ev = reinterpret_cast<float *>(bp + LY::kEvals) - eb;
+    uint32_t *bm = reinterpret_cast<uint32_t *>(bp + LY::kBitmap);
+    const int nwords = (k.e1 - eb + 31) / 32;
+    for (int q = lane; q < nwords; q += 32) bm[q] = 0u;
+    __syncwarp();
+    for (int r = k.r0 + lane; r < k.r1; r += 32) {
+      const int st = max(vp[r], k.e0) - eb;
+      atomicOr(&bm[st >> 5], 1u << (st & 31));
+    }
+    __syncwarp();
+    const unsigned le = lanemask_lt() | (1u << lane);
+    int run = k.r0 - 1;
+    for (int q = 0; q < nwords; ++q) {
+      const uint32_t word = bm[q];
+      const int n = eb + 32 * q + lane;
+      if (n >= k.e0 && n < k.e1) ev[n] = rv[run + __popc(word & le)];
+      run += __popc(word);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ready(s));
+    return true;
+  }
+
   // Producer warp (all lanes; lane 0 issues): fills the ring with blocks
   // b_begin, b_begin + step, ... < b_end, each after the consumers released
-  // its buffer.  Before returning, waits (bounded) until every issued copy has
-  // landed.
+  // its buffer; for VCS it also expands each landed block's run values, one
+  // block behind the newest copy.  Before returning, waits
+  // (bounded) until every issued copy has landed.
   __device__ __forceinline__ void produce(const StageArrays &a, int b_begin, int b_end,
                                           int step) const {
     const int lane = threadIdx.x & 31;
-    int i = 0;
+    int i = 0, done = 0;  // blocks issued, blocks expanded
+    bool ok = true;
     for (int b = b_begin; b < b_end; b += step, ++i) {
       const int s = i % kStages;
       if (i >= kStages && !mbar_wait_bounded(empty(s), ((i / kStages) - 1) & 1, kWaitLimitNs)) {
-        give_up(a);
+        ok = false;
         break;
       }
-      if (*reinterpret_cast<volatile int *>(fail())) break;
+      if (*reinterpret_cast<volatile int *>(fail())) {
+        ok = false;
+        break;
+      }
       if (lane == 0) {
         *counter(s) = 0;
         stage_issue<T, VCS>(a, b, buf(s), full(s));
       }
       __syncwarp();
+      // expand the previous block now (it was issued one round ago), so the
+      // consumers find kStages - 2 expanded blocks ahead of them
+      for (; VCS && done < i; ++done)
+        if (!expand(a, done, b_begin + done * step)) {
+          ok = false;
+          break;
+        }
+      if (!ok) break;
     }
+    if (VCS && ok)
+      for (; done < i; ++done)
+        if (!expand(a, done, b_begin + done * step)) {
+          ok = false;
+          break;
+        }
+    if (!ok) give_up(a);
     if (lane == 0)
       for (int j = i - kStages < 0 ? 0 : i - kStages; j < i; ++j)
         mbar_wait_bounded(full(j % kStages), (j / kStages) & 1, kWaitLimitNs);
@@ -285,7 +349,8 @@ struct Pipe {
 
   // Consumer warp: waits for the i-th block of this CTA; false if the wait gave up.
   __device__ __forceinline__ bool acquire(int i, const StageArrays &a) const {
-    if (mbar_wait_bounded(full(i % kStages), (i / kStages) & 1, kWaitLimitNs)) return true;
+    uint64_t *bar = VCS ? ready(i % kStages) : full(i % kStages);
+    if (mbar_wait_bounded(bar, (i / kStages) & 1, kWaitLimitNs)) return true;
     give_up(a);
     return false;
   }
