@@ -72,15 +72,24 @@ typedef enum { VS_LAYOUT_CSR = 0, VS_LAYOUT_VCS = 1 } vs_layout;
  * Product variants.  Aligned directions always run the deterministic gather;
  * the variant matters only for misaligned directions (VCSC@B, B@VCSR, CSC@B,
  * B@CSR):
- *   VS_DETERMINISTIC  two-phase scheme: per-block partial sums in shared
- *                     memory over tiles of the output, then a combine in a
- *                     fixed chunk order.  Bit-identical on repeats.
+ *   VS_DETERMINISTIC  bit-reproducible: the gather over the exact transpose
+ *                     when the handle holds one (vs_attach_transpose), else the
+ *                     two-phase scheme.
  *   VS_ATOMIC         zero-fill out, then scatter with atomic adds (the pages'
  *                     design); not bit-reproducible.
  *   VS_TRANSPOSED     the aligned gather over the exact transpose held by the
- *                     handle (see vs_attach_transpose); bit-identical on repeats.
+ *                     handle; VS_ERR_INVALID without one.  Bit-identical on
+ *                     repeats.
+ *   VS_TWO_PHASE      per-block partial sums over tiles of the output in
+ *                     shared memory, then a combine in a fixed chunk order.
+ *                     Bit-identical on repeats.
  */
-typedef enum { VS_DETERMINISTIC = 0, VS_ATOMIC = 1, VS_TRANSPOSED = 2 } vs_variant;
+typedef enum {
+    VS_DETERMINISTIC = 0,
+    VS_ATOMIC = 1,
+    VS_TRANSPOSED = 2,
+    VS_TWO_PHASE = 3
+} vs_variant;
 
 typedef struct {
     void *ptr;            /* first element */
@@ -171,9 +180,9 @@ vs_status vs_build_vcs(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_
  * B and out have the handle's dtype; vector loads are used when the width and
  * strides are multiples of 16 bytes and the pointers are 16-byte aligned.
  * w = 0 or an empty matrix returns VS_OK after writing zeros where out has
- * elements.  No allocation happens here for VS_ATOMIC and for aligned
- * directions; VS_DETERMINISTIC on a misaligned direction may grow the
- * handle's scratch on first use with a new width (stream-ordered).  Calls on
+ * elements.  No allocation happens here for VS_ATOMIC, VS_TRANSPOSED and
+ * aligned directions; the two-phase scheme may grow the handle's scratch on
+ * first use with a new width (stream-ordered).  Calls on
  * the same handle must not overlap on the GPU (they share scratch).
  * VS_TRANSPOSED needs vs_attach_transpose first, else VS_ERR_INVALID.
  */
@@ -190,9 +199,10 @@ vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direct
  * callers only.)
  *
  * Arguments, layouts and results as for vs_spmm with VS_DETERMINISTIC: aligned
- * directions run the same gather (which needs no scratch beyond what the
- * handle got at build time), misaligned directions the same two-phase scheme,
- * with its per-group partial sums in a fixed 32 MiB device array that the
+ * directions, and misaligned ones on a handle that holds its transpose, run
+ * the same gather (which needs no scratch beyond what the handle got at build
+ * time); other misaligned products run the same two-phase scheme, with its
+ * per-group partial sums in a fixed 32 MiB device array that the
  * library declares statically -- every GPU that loads the library holds those
  * 32 MiB until the process exits.  Results are bit-identical to vs_spmm's.
  * The column block is narrowed until the partial sums fit; a product whose

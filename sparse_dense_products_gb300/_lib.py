@@ -24,7 +24,7 @@ STATUS = {
 F32, F64 = 0, 1
 MAJOR_ROW, MAJOR_COL = 0, 1
 A_B, B_A = 0, 1
-DETERMINISTIC, ATOMIC, TRANSPOSED = 0, 1, 2
+DETERMINISTIC, ATOMIC, TRANSPOSED, TWO_PHASE = 0, 1, 2, 3
 LAYOUT_CSR, LAYOUT_VCS = 0, 1
 
 

@@ -22,7 +22,8 @@ from . import _lib as L
 _DTYPES = {torch.float32: L.F32, torch.float64: L.F64}
 _MAJORS = {"row": L.MAJOR_ROW, "col": L.MAJOR_COL}
 _DIRS = {"A@B": L.A_B, "B@A": L.B_A}
-_VARIANTS = {"deterministic": L.DETERMINISTIC, "atomic": L.ATOMIC, "transposed": L.TRANSPOSED}
+_VARIANTS = {"deterministic": L.DETERMINISTIC, "atomic": L.ATOMIC, "transposed": L.TRANSPOSED,
+             "two_phase": L.TWO_PHASE}
 
 
 def _stream_ptr(device) -> int:

@@ -166,13 +166,177 @@ struct TwoPhaseArgs {
   int64_t n_t;            // rows of Y
   int tile_rows;          // rows per tile
   int w;
+  int sorted;             // minor indices ascend inside every run / row
 };
+
+// Per-stage record list: the block's entries whose row lies in this CTA's
+// tile, in entry order -- key = tile-relative row | (slice - s0) << 16.
+template <typename T>
+struct RecLayout {
+  static constexpr int kKey = 0;
+  static constexpr int kVal = kKey + kCapEntries * 4;
+  static constexpr int kCount = kVal + kCapEntries * (int)sizeof(T);
+  static constexpr int kBytes = (kCount + 16 + 127) / 128 * 128;
+};
+
+// Producer-side scratch (one per CTA): start bitmaps of slices and runs, and
+// the ids of the non-empty slices of the current block.
+struct PrepLayout {
+  static constexpr int kWords = (kCapEntries + 31) / 32 + 1;
+  static constexpr int kSliceBits = 0;
+  static constexpr int kRunBits = kSliceBits + kWords * 4;
+  static constexpr int kSliceIds = kRunBits + kWords * 4;
+  static constexpr int kBytes = (kSliceIds + kCapSlices * 4 + 127) / 128 * 128;
+};
+
+constexpr int kQueueCap = 64;  // per-warp queue of in-band records
+
+template <typename T, bool VCS>
+struct TwoPhaseSmem {
+  static constexpr int kPipe = 0;
+  static constexpr int kRecs = PipeLayout<T, VCS>::kExtra;
+  static constexpr int kPrep = kRecs + kStages * RecLayout<T>::kBytes;
+  static constexpr int kQueue = kPrep + PrepLayout::kBytes;
+  static constexpr int kTile =
+      kQueue + ((kWarpsPerCta * kQueueCap * (8 + (int)sizeof(T)) + 127) / 128 * 128);
+};
+
+// Producer warp: once block j (number b) has landed, write the records of its
+// entries that fall in rows [t0, t0 + rows), in entry order, and mark the
+// stage ready.  The slice of an entry and (VCS) its run come from start
+// bitmaps counted with popcounts; for sorted runs and a partial tile, only
+// each run's sub-range inside the tile is visited.
+template <typename T, bool VCS>
+__device__ __forceinline__ bool two_phase_prepare(const Pipe<T, VCS> &pipe, const StageArrays &a,
+                                                  int j, int b, unsigned char *recs,
+                                                  unsigned char *prep, int64_t t0, int rows,
+                                                  bool skip_by_search) {
+  using LY = StageLayout<T, VCS>;
+  using RL = RecLayout<T>;
+  const int s = j % kStages;
+  if (!mbar_wait_bounded(pipe.full(s), (j / kStages) & 1, kWaitLimitNs)) return false;
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = lanemask_lt(), le = lt | (1u << lane);
+  const Block k = load_block(a.blocks, b);
+  unsigned char *bp = pipe.buf(s);
+  const Staged<T, VCS> sv = stage_views<T, VCS>(k, bp);
+  const float *rv = VCS ? reinterpret_cast<const float *>(bp + LY::kRvals) - align_down<4>(k.r0)
+                        : nullptr;
+  unsigned char *rb = recs + s * RL::kBytes;
+  uint32_t *key = reinterpret_cast<uint32_t *>(rb + RL::kKey);
+  T *val = reinterpret_cast<T *>(rb + RL::kVal);
+  int *count = reinterpret_cast<int *>(rb + RL::kCount);
+  uint32_t *sbm = reinterpret_cast<uint32_t *>(prep + PrepLayout::kSliceBits);
+  uint32_t *rbm = reinterpret_cast<uint32_t *>(prep + PrepLayout::kRunBits);
+  int32_t *sid = reinterpret_cast<int32_t *>(prep + PrepLayout::kSliceIds);
+  const int eb = align_down<4>(k.e0);
+  const int nwords = (k.e1 - eb + 31) / 32;
+  int nrec = 0;
+
+  // slice and run start bitmaps over the block's entries
+  for (int q = lane; q < nwords; q += 32) {
+    sbm[q] = 0u;
+    if (VCS) rbm[q] = 0u;
+  }
+  __syncwarp();
+  int ns = 0;  // non-empty slices, in order
+  if (k.type == 0) {
+    for (int base = k.s0; base < k.s1; base += 32) {
+      const int sl = base + lane;
+      const bool ne = sl < k.s1 &&
+                      (VCS ? sv.vptr[sv.ptr[sl]] < sv.vptr[sv.ptr[sl + 1]] : sv.ptr[sl] < sv.ptr[sl + 1]);
+      const unsigned m = __ballot_sync(kFullMask, ne);
+      if (ne) {
+        sid[ns + __popc(m & lt)] = sl - k.s0;
+        const int st = (VCS ? sv.vptr[sv.ptr[sl]] : sv.ptr[sl]) - eb;
+        atomicOr(&sbm[st >> 5], 1u << (st & 31));
+      }
+      ns += __popc(m);
+    }
+  } else {
+    if (lane == 0) {
+      sid[0] = 0;
+      const int st = k.e0 - eb;
+      sbm[st >> 5] |= 1u << (st & 31);
+    }
+    ns = 1;
+  }
+  if (VCS) {
+    for (int r = k.r0 + lane; r < k.r1; r += 32) {
+      const int st = max(sv.vptr[r], k.e0) - eb;
+      atomicOr(&rbm[st >> 5], 1u << (st & 31));
+    }
+  }
+  __syncwarp();
+
+  if (!(VCS && skip_by_search)) {
+    // every entry of the block, 32 at a time
+    int sbase = -1, rbase = k.r0 - 1;
+    for (int q = 0; q < nwords; ++q) {
+      const int n = eb + 32 * q + lane;
+      const uint32_t sw = sbm[q];
+      const uint32_t rw = VCS ? rbm[q] : 0u;
+      const int sidx = sbase + __popc(sw & le);
+      const int ridx = rbase + __popc(rw & le);
+      sbase += __popc(sw);
+      rbase += __popc(rw);
+      bool in = false;
+      int tt = 0;
+      if (n >= k.e0 && n < k.e1) {
+        tt = (int)(sv.idx[n] - t0);
+        in = tt >= 0 && tt < rows;
+      }
+      const unsigned m = __ballot_sync(kFullMask, in);
+      if (in) {
+        const int pos = nrec + __popc(m & lt);
+        key[pos] = (uint32_t)tt | ((uint32_t)sid[sidx] << 16);
+        val[pos] = VCS ? (T)rv[ridx] : sv.vals[n];
+      }
+      nrec += __popc(m);
+    }
+  } else {
+    // sorted runs, partial tile: per run, only the entries inside [t0, t0 + rows)
+    int cur_slice = 0;  // index into sid
+    for (int r = k.r0; r < k.r1; ++r) {
+      int lo = max(sv.vptr[r], k.e0), hi = min(sv.vptr[r + 1], k.e1);
+      while (cur_slice + 1 < ns) {  // the slice holding run r's first entry
+        const int nxt = k.type == 0 ? sv.vptr[sv.ptr[k.s0 + sid[cur_slice + 1]]] : k.e1;
+        if (nxt <= lo) ++cur_slice;
+        else break;
+      }
+      // first entry with row >= t0, then first with row >= t0 + rows
+      int a0 = lo, a1 = hi;
+      while (a0 < a1) {
+        const int mid = (a0 + a1) >> 1;
+        if (sv.idx[mid] < t0) a0 = mid + 1;
+        else a1 = mid;
+      }
+      int b0 = a0, b1 = hi;
+      while (b0 < b1) {
+        const int mid = (b0 + b1) >> 1;
+        if (sv.idx[mid] < t0 + rows) b0 = mid + 1;
+        else b1 = mid;
+      }
+      const uint32_t sk = (uint32_t)sid[cur_slice] << 16;
+      const T v = (T)rv[r];
+      for (int n = a0 + lane; n < b0; n += 32) {
+        key[nrec + n - a0] = (uint32_t)(sv.idx[n] - t0) | sk;
+        val[nrec + n - a0] = v;
+      }
+      nrec += b0 - a0;
+    }
+  }
+  if (lane == 0) *count = nrec;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(pipe.ready(s));
+  return true;
+}
 
 template <typename T, int VEC, int Q, int CI, bool VCS>
 struct TwoPhaseWarp {
   using V = typename VecT<T, VEC>::type;
   using Ops = VecOps<T, VEC>;
-  static constexpr int E = 32 / Q;  // entries applied per step
+  static constexpr int E = 32 / Q;  // records applied per step
 
   __device__ __forceinline__ static void apply(T *tile, int w, int tk, T ak, const T (&x)[CI][VEC],
                                                const int (&col0)[CI], const bool (&colok)[CI]) {
@@ -188,78 +352,78 @@ struct TwoPhaseWarp {
     }
   }
 
-  // Applies the entries [n0, n1) of slice s whose rows fall in this warp's
-  // band [lo, hi) (tile-relative), in entry order.
-  __device__ __forceinline__ static void run(const Staged<T, VCS> &sv, const T *__restrict__ X,
-                                             int64_t ldx, T *tile, int w, int64_t t0, int lo,
-                                             int hi, int s, int n0, int n1, int rlo, int rhi,
+  // Applies, in record order, the records [0, nrec) whose row lies in this
+  // warp's band [lo, hi) of the tile.
+  __device__ __forceinline__ static void run(const uint32_t *key, const T *val, int nrec, int s0,
+                                             const T *__restrict__ X, int64_t ldx, T *tile, int w,
+                                             int lo, int hi, uint32_t *qkey, T *qval,
                                              const int (&col0)[CI], const bool (&colok)[CI]) {
     const int lane = threadIdx.x & 31, grp = lane / Q;
-    T x[CI][VEC];
-#pragma unroll
-    for (int ci = 0; ci < CI; ++ci)
-      if (colok[ci])
-        Ops::unpack(ld_gather(reinterpret_cast<const V *>(X + (int64_t)s * ldx + col0[ci])), x[ci]);
-    for (int base = n0; base < n1; base += 32) {
-      const int n = base + lane;
-      int t = -1;
-      T av = T(0);
-      if (n < n1) {
-        const int tt = (int)(sv.idx[n] - t0);
-        if (tt >= lo && tt < hi) {
-          t = tt;
-          if (VCS) {  // the run of entry n
-            int a0 = rlo, a1 = rhi - 1;
-            while (a0 < a1) {
-              const int mid = (a0 + a1 + 1) >> 1;
-              if (sv.vptr[mid] <= n) a0 = mid;
-              else a1 = mid - 1;
-            }
-            av = (T)sv.rvals[a0];
-          } else {
-            av = sv.vals[n];
-          }
-        }
+    const unsigned lt = lanemask_lt();
+    for (int base = 0; base < nrec; base += 32) {
+      const int r = base + lane;
+      uint32_t kk = 0;
+      bool in = false;
+      if (r < nrec) {
+        kk = key[r];
+        const int t = (int)(kk & 0xffffu);
+        in = t >= lo && t < hi;
       }
-      unsigned bits = __ballot_sync(kFullMask, t >= 0);
-      while (bits) {
-        const int cnt = min(E, __popc(bits));
-        int src = 0;
-        if (grp < cnt) {
-          unsigned bb = bits;
-          for (int q = 0; q < grp; ++q) bb &= bb - 1;  // drop the grp lowest set bits
-          src = __ffs(bb) - 1;
+      const unsigned m = __ballot_sync(kFullMask, in);
+      if (in) {  // compact the in-band records into the warp's queue, in order
+        const int p = __popc(m & lt);
+        qkey[p] = kk;
+        qval[p] = val[r];
+      }
+      __syncwarp();
+      const int cnt = __popc(m);
+      for (int c0 = 0; c0 < cnt; c0 += E) {
+        const int qi = c0 + grp;
+        int tk = -1;
+        T ak = T(0);
+        T x[CI][VEC];
+        if (qi < cnt) {
+          const uint32_t q = qkey[qi];
+          tk = (int)(q & 0xffffu);
+          ak = qval[qi];
+          const int sl = s0 + (int)(q >> 16);
+#pragma unroll
+          for (int ci = 0; ci < CI; ++ci)
+            if (colok[ci])
+              Ops::unpack(ld_gather(reinterpret_cast<const V *>(X + (int64_t)sl * ldx + col0[ci])),
+                          x[ci]);
         }
-        int tk = __shfl_sync(kFullMask, t, src);
-        const T ak = __shfl_sync(kFullMask, av, src);
-        if (grp >= cnt) tk = -1;
-        for (int q = 0; q < cnt; ++q) bits &= bits - 1;
         const unsigned peers = __match_any_sync(kFullMask, tk);
         const bool dup = tk >= 0 && __popc(peers) > Q;
         if (!__any_sync(kFullMask, dup)) {
           if (tk >= 0) apply(tile, w, tk, ak, x, col0, colok);
-          __syncwarp();
         } else {
-          // equal rows inside the step: one round per earlier duplicate, in entry order
-          const int rank = __popc(peers & lanemask_lt()) / Q;
+          // equal rows inside the step: one round per earlier duplicate, in record order
+          const int rank = __popc(peers & lt) / Q;
           for (int rd = 0; rd < E; ++rd) {
             if (tk >= 0 && rank == rd) apply(tile, w, tk, ak, x, col0, colok);
             __syncwarp();
           }
         }
       }
+      __syncwarp();
     }
   }
 };
 
-// Block (tile blockIdx.x, group blockIdx.y).  Every consumer warp walks all
-// blocks of the group in order (for its own band of the tile's rows).
+// Block (tile blockIdx.x, group blockIdx.y).  The producer warp streams the
+// group's blocks and turns each into the records of this tile; consumer warp w
+// applies the records of its band of the tile's rows.
 template <typename T, int VEC, int Q, int CI, bool VCS>
 __global__ void __launch_bounds__(kPipeThreads) two_phase_kernel(const TwoPhaseArgs a) {
   using WP = TwoPhaseWarp<T, VEC, Q, CI, VCS>;
+  using SM = TwoPhaseSmem<T, VCS>;
+  using RL = RecLayout<T>;
   extern __shared__ __align__(128) unsigned char smem[];
   const Pipe<T, VCS> pipe{smem};
-  T *tile = reinterpret_cast<T *>(smem + PipeLayout<T, VCS>::kExtra);
+  unsigned char *recs = smem + SM::kRecs;
+  unsigned char *prep = smem + SM::kPrep;
+  T *tile = reinterpret_cast<T *>(smem + SM::kTile);
 
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int64_t t0 = (int64_t)blockIdx.x * a.tile_rows;
@@ -268,8 +432,33 @@ __global__ void __launch_bounds__(kPipeThreads) two_phase_kernel(const TwoPhaseA
   const int b_lo = a.bounds[blockIdx.y], b_hi = a.bounds[blockIdx.y + 1];
   for (int q = threadIdx.x; q < rows * w; q += kPipeThreads) tile[q] = T(0);
   pipe.init();  // (its barrier also publishes the zeroed tile)
-  if (wid == kWarpsPerCta) {  // the producer warp
-    pipe.produce(a.st, b_lo, b_hi, 1);
+  if (wid == kWarpsPerCta) {
+    // ---- producer: issue block i, then prepare block i - 1
+    const bool search = VCS && a.sorted && rows < a.n_t;
+    int i = 0, done = 0;
+    bool ok = true;
+    for (int b = b_lo; b < b_hi; ++b, ++i) {
+      const int st = i % kStages;
+      if (i >= kStages && !mbar_wait_bounded(pipe.empty(st), ((i / kStages) - 1) & 1, kWaitLimitNs)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) stage_issue<T, VCS>(a.st, b, pipe.buf(st), pipe.full(st));
+      __syncwarp();
+      for (; done < i; ++done)
+        if (!two_phase_prepare<T, VCS>(pipe, a.st, done, b_lo + done, recs, prep, t0, rows, search)) {
+          ok = false;
+          break;
+        }
+      if (!ok) break;
+    }
+    for (; ok && done < i; ++done)
+      if (!two_phase_prepare<T, VCS>(pipe, a.st, done, b_lo + done, recs, prep, t0, rows, search))
+        ok = false;
+    if (!ok) pipe.give_up(a.st);
+    if (lane == 0)
+      for (int j = i - kStages < 0 ? 0 : i - kStages; j < i; ++j)
+        mbar_wait_bounded(pipe.full(j % kStages), (j / kStages) & 1, kWaitLimitNs);
   } else {
     const int band = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
     const int lo = min(rows, wid * band), hi = min(rows, lo + band);
@@ -282,31 +471,23 @@ __global__ void __launch_bounds__(kPipeThreads) two_phase_kernel(const TwoPhaseA
       colok[ci] = col0[ci] < w;
     }
     const T *__restrict__ X = static_cast<const T *>(a.X);
+    unsigned char *qbase = smem + SM::kQueue + wid * kQueueCap * (8 + (int)sizeof(T));
+    uint32_t *qkey = reinterpret_cast<uint32_t *>(qbase);
+    T *qval = reinterpret_cast<T *>(qbase + kQueueCap * 8);
     int i = 0;
     for (int b = b_lo; b < b_hi; ++b, ++i) {
-      if (!pipe.acquire(i, a.st)) break;
-      const Block k = load_block(a.st.blocks, b);
-      const Staged<T, VCS> sv = stage_views<T, VCS>(k, pipe.buf(i % kStages));
-      if (lo < hi) {
-        if (k.type == 0) {
-          for (int s = k.s0; s < k.s1; ++s) {
-            int n0, n1, rlo = 0, rhi = 0;
-            if (VCS) {
-              rlo = sv.ptr[s];
-              rhi = sv.ptr[s + 1];
-              n0 = sv.vptr[rlo];
-              n1 = sv.vptr[rhi];
-            } else {
-              n0 = sv.ptr[s];
-              n1 = sv.ptr[s + 1];
-            }
-            if (n0 < n1)
-              WP::run(sv, X, a.ldx, tile, w, t0, lo, hi, s, n0, n1, rlo, rhi, col0, colok);
-          }
-        } else {
-          WP::run(sv, X, a.ldx, tile, w, t0, lo, hi, k.s0, k.e0, k.e1, k.r0, k.r1, col0, colok);
-        }
+      const int st = i % kStages;
+      if (!mbar_wait_bounded(pipe.ready(st), (i / kStages) & 1, kWaitLimitNs)) {
+        pipe.give_up(a.st);
+        break;
       }
+      const Block k = load_block(a.st.blocks, b);
+      const unsigned char *rb = recs + st * RL::kBytes;
+      if (lo < hi)
+        WP::run(reinterpret_cast<const uint32_t *>(rb + RL::kKey),
+                reinterpret_cast<const T *>(rb + RL::kVal),
+                *reinterpret_cast<const int *>(rb + RL::kCount), k.s0, X, a.ldx, tile, w, lo, hi,
+                qkey, qval, col0, colok);
       pipe.release(i);
     }
   }
@@ -451,7 +632,7 @@ vs_status two_phase_typed(vs_handle_s &h, const Matrix &m, DenseView X, DenseVie
                           cudaStream_t s) {
   const int C = m.tp_chunks;
   const int64_t n_t = Y.rows;
-  constexpr int stage = pipe_smem_bytes<T, VCS>(0);
+  constexpr int stage = TwoPhaseSmem<T, VCS>::kTile;
   for (int64_t c0 = 0; c0 < w; c0 += kMaxBlockWidth) {
     const int wb = (int)std::min<int64_t>(kMaxBlockWidth, w - c0);
     const T *xp = static_cast<const T *>(X.p) + c0;
@@ -477,6 +658,7 @@ vs_status two_phase_typed(vs_handle_s &h, const Matrix &m, DenseView X, DenseVie
     a.n_t = n_t;
     a.tile_rows = tile_rows;
     a.w = wb;
+    a.sorted = m.sorted_segments ? 1 : 0;
     if (C == 1) {
       a.out = yp;
       a.ldo = Y.ld;
@@ -543,7 +725,7 @@ vs_status two_phase_static_typed(const Matrix &m, DenseView X, DenseView Y, int6
                                  cudaStream_t s) {
   const int C = m.tp_chunks;
   const int64_t n_t = Y.rows;
-  constexpr int stage = pipe_smem_bytes<T, VCS>(0);
+  constexpr int stage = TwoPhaseSmem<T, VCS>::kTile;
   constexpr int VW = 16 / sizeof(T);
   void *scratch = nullptr;
   int64_t wmax = kMaxBlockWidth;
@@ -584,6 +766,7 @@ vs_status two_phase_static_typed(const Matrix &m, DenseView X, DenseView Y, int6
     a.n_t = n_t;
     a.tile_rows = tile_rows;
     a.w = wb;
+    a.sorted = m.sorted_segments ? 1 : 0;
     if (C == 1) {
       a.out = yp;
       a.ldo = Y.ld;

@@ -214,7 +214,8 @@ vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direct
                   vs_variant variant, cudaStream_t stream) {
   if (!valid_handle(A)) return invalid("NULL handle");
   if (!B || !out) return invalid("NULL operand descriptor");
-  if (variant != VS_DETERMINISTIC && variant != VS_ATOMIC && variant != VS_TRANSPOSED)
+  if (variant != VS_DETERMINISTIC && variant != VS_ATOMIC && variant != VS_TRANSPOSED &&
+      variant != VS_TWO_PHASE)
     return invalid("unknown variant");
   DenseView X, Y;
   int64_t w = 0;
@@ -228,7 +229,10 @@ vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direct
     case VS_TRANSPOSED:
       if (!A->T) return invalid("VS_TRANSPOSED needs vs_attach_transpose first");
       return launch_gather(*A->T, X, Y, w, stream);
-    default:
+    case VS_TWO_PHASE:
+      return launch_scatter_two_phase(*A, A->A, X, Y, w, stream);
+    default:  // VS_DETERMINISTIC
+      if (A->T) return launch_gather(*A->T, X, Y, w, stream);
       return launch_scatter_two_phase(*A, A->A, X, Y, w, stream);
   }
 }
@@ -243,6 +247,7 @@ vs_status vs_spmm_noalloc(vs_handle A, const vs_dense *B, const vs_dense *out, v
   VS_TRY(frame(A->A, *B, *out, dir, X, Y, w, aligned));
   if (w == 0 || Y.rows == 0) return VS_OK;
   if (aligned) return launch_gather(A->A, X, Y, w, stream);
+  if (A->T) return launch_gather(*A->T, X, Y, w, stream);
   return launch_scatter_two_phase_static(A->A, X, Y, w, stream);
 }
 

@@ -30,8 +30,8 @@ def _cuda():
 
 
 def _variants(major, direction):
-    return ["deterministic"] if aligned(major, direction) else ["deterministic", "atomic",
-                                                                "transposed"]
+    return ["deterministic"] if aligned(major, direction) else ["deterministic", "two_phase",
+                                                                "atomic", "transposed"]
 
 
 def _run(A, B, direction, variant):
@@ -231,7 +231,8 @@ def test_strided_operands_and_layout_errors():
 def test_repeats_bit_identical_and_column_alone_equals_batch(layout, major, direction):
     coo = workload("tiny")
     A = build(coo, layout, major)
-    variants = ["deterministic"] if aligned(major, direction) else ["deterministic", "transposed"]
+    variants = (["deterministic"] if aligned(major, direction)
+                else ["deterministic", "two_phase", "transposed"])
     B, _ = dense_operand(coo, direction, 33, torch.float32)
     for variant in variants:
         ref = _run(A, B, direction, variant).clone()
@@ -254,7 +255,7 @@ def test_atomic_and_deterministic_agree_within_tolerance_on_main_workload():
         B, Bt = dense_operand(coo, direction, 16, torch.float32)
         tri = oracle_triples(coo, layout, major)
         want, D = oracle_product(coo, tri, direction, Bt)
-        for variant in ("deterministic", "atomic", "transposed"):
+        for variant in ("deterministic", "two_phase", "atomic", "transposed"):
             got = gpu_out_rows(_run(A, B, direction, variant), direction)
             assert_close(got, want, D, 1e-5, f"main {layout}/{major} {direction} {variant}")
         A.destroy()
@@ -288,7 +289,8 @@ def test_regrid_workload(dtype, direction):
     for w in (1, 4, 32):
         B, Bt = dense_operand(coo, direction, w, dtype)
         want, D = oracle_product(coo, tri, direction, Bt)
-        variants = ["deterministic"] if direction == "A@B" else ["deterministic", "atomic", "transposed"]
+        variants = (["deterministic"] if direction == "A@B"
+                    else ["deterministic", "two_phase", "atomic", "transposed"])
         for variant in variants:
             out = _run(A, B, direction, variant)
             got = gpu_out_rows(out, direction)
