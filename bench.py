@@ -350,6 +350,24 @@ def gpu_arm(args):
             vb = product_bytes(layout, major, direction, variant)
             variants[f"{name}/{variant}"] = {"ms": round(ms, 5), "GBs": round(vb / ms / 1e6, 1)}
 
+    # ---- in-run cuSPARSE reference: torch's CSR matmul on the index-sorted CSR
+    # (CSR@B), and on the CSR of the exact transpose for B@CSR (Y^T = A^T B^T)
+    cusparse = {}
+    try:
+        a = handles[("csr", "row")].arrays()
+        A_csr = torch.sparse_csr_tensor(a["ptr"], a["indices"], a["values"], (n_rows, n_cols))
+        with vs.build_csr(coo.cols, coo.rows, coo.vals, (n_cols, n_rows), "row") as hT:
+            t = hT.arrays()
+        AT_csr = torch.sparse_csr_tensor(t["ptr"], t["indices"], t["values"], (n_cols, n_rows))
+        for name, Am, X in (("CSR@B", A_csr, Bab), ("B@CSR", AT_csr, Bt)):
+            torch.mm(Am, X)
+            ts = timed(lambda: torch.mm(Am, X), max(5, args.steps))
+            ms = statistics.mean(ts)
+            cusparse[name] = {"ms": round(ms, 5), "GBs": round(nbytes[name] / ms / 1e6, 1),
+                              "ours_over_cusparse_time": round(ms_prod[name] / ms, 3)}
+    except Exception as exc:  # reported, never fatal: it is a comparison, not the path
+        cusparse = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
+
     # ---- e2e through vs_spmm_host with pinned host buffers
     Bab_h = Bab.cpu().pin_memory()
     Bt_h = Bt.cpu().pin_memory()
@@ -415,6 +433,7 @@ def gpu_arm(args):
         "gpu_launches": launches,
         "products": products,
         "misaligned_variants": variants,
+        "cusparse": cusparse,
         "assembly_ms": assembly,
         "wall_s_timed_region": round(wall, 3),
     }

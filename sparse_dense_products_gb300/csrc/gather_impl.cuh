@@ -40,6 +40,10 @@
 
 #include "stage.cuh"
 
+#ifndef VS_GATHER_MIN_CTAS
+#define VS_GATHER_MIN_CTAS 3
+#endif
+
 namespace vs {
 namespace gather_detail {
 
@@ -50,6 +54,7 @@ struct GatherArgs {
   void *Y;
   int64_t ldy;
   int w;           // columns in this launch (<= kMaxBlockWidth)
+  int n_x;         // rows of X (shared-memory variant: rows copied into the slab)
   void *partials;  // [n_shares][kMaxBlockWidth] of T
   int *counters;   // [n_long]
 };
@@ -60,13 +65,36 @@ __device__ __forceinline__ int atomic_add_release(int *p, int v) {
   return old;
 }
 
-// Sums entries [n0, n1) of one slice for the column tile starting at `col`
-// (this lane's VEC columns) and runs the fixed tree; acc[0] holds the result
-// in the slice's slot-0 lanes.
-template <typename T, int VEC, int Q, int G, int NP, bool VCS>
-__device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const T *__restrict__ Xc,
-                                             int64_t ldx, int n0, int n1, int slot, bool cok,
-                                             T (&acc)[NP][VEC]) {
+// Where the rows X[t, :] come from.  Each lane holds the address of its own
+// VEC columns in row 0 (a valid column even for lanes past the width, whose
+// results are never stored, so loads need no predicate).
+template <typename T, int VEC, bool XS>
+struct XSource;
+// Through L1: X in global memory, row stride `ldb` bytes.
+template <typename T, int VEC>
+struct XSource<T, VEC, false> {
+  using V = typename VecT<T, VEC>::type;
+  const char *base;
+  uint32_t ldb;
+  __device__ __forceinline__ V load(int t) const {
+    return ld_gather(reinterpret_cast<const V *>(base + (size_t)(uint32_t)t * ldb));
+  }
+};
+// Shared memory: a slab of X whose rows hold one column pass (Q * VEC
+// elements), copied in once per CTA.
+template <typename T, int VEC>
+struct XSource<T, VEC, true> {
+  using V = typename VecT<T, VEC>::type;
+  uint32_t base;
+  uint32_t row;  // bytes per slab row
+  __device__ __forceinline__ V load(int t) const { return ld_shared<V>(base + (uint32_t)t * row); }
+};
+
+// Sums entries [n0, n1) of one slice for this lane's VEC columns and runs the
+// fixed tree; acc[0] holds the result in the slice's slot-0 lanes.
+template <typename T, int VEC, int Q, int G, int NP, bool VCS, class XSrc>
+__device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const XSrc &xs, int n0,
+                                             int n1, int slot, T (&acc)[NP][VEC]) {
   using V = typename VecT<T, VEC>::type;
   using Ops = VecOps<T, VEC>;
   constexpr int STEP = G * NP;
@@ -88,8 +116,7 @@ __device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const T *
     }
     V x[2 * NP];
 #pragma unroll
-    for (int i = 0; i < 2 * NP; ++i)
-      x[i] = cok ? ld_gather(reinterpret_cast<const V *>(Xc + (int64_t)j[i] * ldx)) : V{};
+    for (int i = 0; i < 2 * NP; ++i) x[i] = xs.load(j[i]);
 #pragma unroll
     for (int i = 0; i < 2 * NP; ++i) {  // step it, then step it + 1, partial by partial
       T xe[VEC];
@@ -108,8 +135,7 @@ __device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const T *
     }
     V x[NP];
 #pragma unroll
-    for (int i = 0; i < NP; ++i)
-      x[i] = cok ? ld_gather(reinterpret_cast<const V *>(Xc + (int64_t)j[i] * ldx)) : V{};
+    for (int i = 0; i < NP; ++i) x[i] = xs.load(j[i]);
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
       T xe[VEC];
@@ -125,7 +151,7 @@ __device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const T *
     if (nn < n1) {
       const int jj = sv.idx[nn];
       const T a = sv.vals[nn];
-      const V x = cok ? ld_gather(reinterpret_cast<const V *>(Xc + (int64_t)jj * ldx)) : V{};
+      const V x = xs.load(jj);
       T xe[VEC];
       Ops::unpack(x, xe);
 #pragma unroll
@@ -146,21 +172,45 @@ __device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const T *
       acc[0][e] = acc[0][e] + __shfl_xor_sync(kFullMask, acc[0][e], sft * Q);
 }
 
-#ifndef VS_GATHER_MIN_CTAS
-#define VS_GATHER_MIN_CTAS 3
-#endif
-template <typename T, int VEC, int Q, int G, int NP, bool VCS>
-__global__ void __launch_bounds__(kPipeThreads, VS_GATHER_MIN_CTAS) gather_kernel(const GatherArgs a) {
+// Launch shape: XS = false gathers X through L1 (8 consumer warps, 4 stage
+// buffers, 3 CTAs per SM, one producer warp); XS = true keeps X in shared
+// memory (16 consumer warps, 8 stage buffers, one CTA per SM, the slab taking
+// the rest of the SM's shared memory).  With one CTA per SM a single warp
+// cannot keep up with expanding VCS run values, so XS with VCS splits the
+// producer into one issuing warp and kExpanders expanding warps.
+template <bool XS, bool VCS>
+struct GatherShape {
+  static constexpr int kWarps = XS ? 16 : kWarpsPerCta;
+  static constexpr int kStageBufs = XS ? 8 : kStages;
+  static constexpr int kExpanders = XS && VCS ? 4 : 0;
+  static constexpr int kThreads = (kWarps + 1 + kExpanders) * 32;
+  static constexpr int kMinCtas = XS ? 1 : VS_GATHER_MIN_CTAS;
+  static_assert(kExpanders == 0 || kStageBufs % kExpanders == 0,
+                "each stage buffer must always go to the same expanding warp");
+};
+
+template <typename T, int VEC, int Q, int G, int NP, bool VCS, bool XS>
+__global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS, VCS>::kMinCtas)
+    gather_kernel(const GatherArgs a) {
   using V = typename VecT<T, VEC>::type;
   using Ops = VecOps<T, VEC>;
+  using Shape = GatherShape<XS, VCS>;
+  constexpr int NW = Shape::kWarps;
+  constexpr int NS = Shape::kStageBufs;
   constexpr int S = 32 / (Q * G);  // slices per warp work unit
   constexpr int TW = Q * VEC;      // columns per pass
   extern __shared__ __align__(128) unsigned char smem[];
-  const Pipe<T, VCS> pipe{smem};
-  pipe.init();
+  const Pipe<T, VCS, NS> pipe{smem};
+  pipe.init(NW);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (wid == kWarpsPerCta) {  // the producer warp
-    pipe.produce(a.st, blockIdx.x, a.st.n_blocks, gridDim.x);
+  if (wid >= NW) {  // the producer warp(s)
+    if constexpr (Shape::kExpanders == 0)
+      pipe.produce(a.st, blockIdx.x, a.st.n_blocks, gridDim.x);
+    else if (wid == NW)
+      pipe.issue_all(a.st, blockIdx.x, a.st.n_blocks, gridDim.x);
+    else
+      pipe.expand_share(a.st, blockIdx.x, a.st.n_blocks, gridDim.x, wid - NW - 1,
+                        Shape::kExpanders);
     return;
   }
   const int ql = lane % Q;
@@ -170,19 +220,46 @@ __global__ void __launch_bounds__(kPipeThreads, VS_GATHER_MIN_CTAS) gather_kerne
   T *__restrict__ Y = static_cast<T *>(a.Y);
   T *__restrict__ P = static_cast<T *>(a.partials);
   const int w = a.w;
+  const int npass = (w + TW - 1) / TW;
 
-  int i = 0, rot = 0;  // rot: units handed out so far, mod kWarpsPerCta
+  // XS: copy X[:, 0:w) into the slab, pass by pass ([pass][row][TW], columns
+  // past w zero), while the producer already streams the first blocks
+  T *slab = reinterpret_cast<T *>(smem + PipeLayout<T, VCS, NS>::kExtra);
+  if constexpr (XS) {
+    const int nv = a.n_x * Q;  // vectors per pass
+    for (int p = 0; p < npass; ++p)
+      for (int v = threadIdx.x; v < nv; v += NW * 32) {
+        const int r = v / Q, c = p * TW + (v % Q) * VEC;
+        V x{};
+        if (c < w) x = ld_gather(reinterpret_cast<const V *>(X + (int64_t)r * a.ldx + c));
+        *reinterpret_cast<V *>(slab + ((int64_t)p * a.n_x + r) * TW + (v % Q) * VEC) = x;
+      }
+    named_barrier(1, NW * 32);
+  }
+  auto source = [&](int cp) {
+    // this lane's columns in pass cp / TW; lanes past the width read column 0
+    const int col = cp + ql * VEC < w ? ql * VEC : 0;
+    if constexpr (XS) {
+      return XSource<T, VEC, true>{
+          smem_u32(slab + (size_t)(cp / TW) * a.n_x * TW + col), (uint32_t)(TW * sizeof(T))};
+    } else {
+      return XSource<T, VEC, false>{reinterpret_cast<const char *>(X + cp + col),
+                                    (uint32_t)(a.ldx * (int64_t)sizeof(T))};
+    }
+  };
+
+  int i = 0, rot = 0;  // rot: units handed out so far, mod NW
   for (int b = blockIdx.x; b < a.st.n_blocks; b += gridDim.x, ++i) {
     if (!pipe.acquire(i, a.st)) return;
-    const Block k = load_block(a.st.blocks, b);
-    unsigned char *buf = pipe.buf(i % kStages);
+    unsigned char *buf = pipe.buf(i % NS);
+    const Block k = stage_desc<T, VCS>(buf);
     const Staged<T, VCS> sv = stage_views<T, VCS>(k, buf);
     const int units = block_units(k, S);
     T acc[NP][VEC];
     // work units go round-robin to the consumer warps, continuing across blocks
-    const int u0 = (wid - rot + kWarpsPerCta) % kWarpsPerCta;
-    rot = (rot + units) % kWarpsPerCta;
-    for (int u = u0; u < units; u += kWarpsPerCta) {
+    const int u0 = (wid - rot + NW) % NW;
+    rot = (rot + units) % NW;
+    for (int u = u0; u < units; u += NW) {
       if (k.type == 0) {
         // ---- S consecutive slices, one per sub-group
         const int sa = k.s0 + u * S;
@@ -193,11 +270,10 @@ __global__ void __launch_bounds__(kPipeThreads, VS_GATHER_MIN_CTAS) gather_kerne
           n0 = VCS ? sv.vptr[sv.ptr[s]] : sv.ptr[s];
           n1 = VCS ? sv.vptr[sv.ptr[s + 1]] : sv.ptr[s + 1];
         }
-        for (int cp = 0; cp < w; cp += TW) {
+        for (int cp = 0; cp < npass * TW; cp += TW) {
           const int col = cp + ql * VEC;
-          const bool cok = col < w;
-          gather_range<T, VEC, Q, G, NP, VCS>(sv, X + col, a.ldx, n0, n1, slot, cok, acc);
-          if (mine && slot == 0 && cok)
+          gather_range<T, VEC, Q, G, NP, VCS>(sv, source(cp), n0, n1, slot, acc);
+          if (mine && slot == 0 && col < w)
             *reinterpret_cast<V *>(Y + (int64_t)s * a.ldy + col) = Ops::pack(acc[0]);
         }
       } else {
@@ -205,11 +281,10 @@ __global__ void __launch_bounds__(kPipeThreads, VS_GATHER_MIN_CTAS) gather_kerne
         // share of the slice to arrive adds all of them in share order
         const int na = k.e0 + u * kShareEntries, nb = min(k.e1, na + kShareEntries);
         const int n0 = sub == 0 ? na : 0, n1 = sub == 0 ? nb : 0;
-        for (int cp = 0; cp < w; cp += TW) {
+        for (int cp = 0; cp < npass * TW; cp += TW) {
           const int col = cp + ql * VEC;
-          const bool cok = col < w;
-          gather_range<T, VEC, Q, G, NP, VCS>(sv, X + col, a.ldx, n0, n1, slot, cok, acc);
-          if (sub == 0 && slot == 0 && cok)
+          gather_range<T, VEC, Q, G, NP, VCS>(sv, source(cp), n0, n1, slot, acc);
+          if (sub == 0 && slot == 0 && col < w)
             *reinterpret_cast<V *>(P + (int64_t)(k.first + u) * kMaxBlockWidth + col) =
                 Ops::pack(acc[0]);
         }
@@ -245,61 +320,105 @@ using KernelPtr = void (*)(const GatherArgs);
 #endif
 constexpr int kMaxSlots = VS_MAX_SLOTS;
 
-template <typename T, int VEC, int Q, int G, bool VCS>
+template <typename T, int VEC, int Q, int G, bool VCS, bool XS>
 KernelPtr<T, VCS> pick_np(int np) {
   if constexpr (G == kMaxSlots || G * Q == 32) {
     if constexpr (Q * G * 2 <= 64)
-      if (np == 2) return gather_kernel<T, VEC, Q, G, 2, VCS>;
+      if (np == 2) return gather_kernel<T, VEC, Q, G, 2, VCS, XS>;
     if constexpr (Q * G * 4 <= 128)
-      if (np == 4) return gather_kernel<T, VEC, Q, G, 4, VCS>;
+      if (np == 4) return gather_kernel<T, VEC, Q, G, 4, VCS, XS>;
   }
-  return np == 1 ? gather_kernel<T, VEC, Q, G, 1, VCS> : nullptr;
+  return np == 1 ? gather_kernel<T, VEC, Q, G, 1, VCS, XS> : nullptr;
 }
 
-template <typename T, int VEC, int Q, bool VCS>
+template <typename T, int VEC, int Q, bool VCS, bool XS>
 KernelPtr<T, VCS> pick_g(int G, int np) {
   switch (G) {
-    case 1: return pick_np<T, VEC, Q, 1, VCS>(np);
-    case 2: return pick_np<T, VEC, Q, 2, VCS>(np);
-    case 4: return pick_np<T, VEC, Q, 4, VCS>(np);
-    case 8: return pick_np<T, VEC, Q, 8, VCS>(np);
-    case 16: if constexpr (kMaxSlots >= 16 && Q <= 2) return pick_np<T, VEC, Q, 16, VCS>(np); break;
-    case 32: if constexpr (kMaxSlots >= 32 && Q == 1) return pick_np<T, VEC, Q, 32, VCS>(np); break;
+    case 1: return pick_np<T, VEC, Q, 1, VCS, XS>(np);
+    case 2: return pick_np<T, VEC, Q, 2, VCS, XS>(np);
+    case 4: return pick_np<T, VEC, Q, 4, VCS, XS>(np);
+    case 8: return pick_np<T, VEC, Q, 8, VCS, XS>(np);
+    case 16: if constexpr (kMaxSlots >= 16 && Q <= 2) return pick_np<T, VEC, Q, 16, VCS, XS>(np); break;
+    case 32: if constexpr (kMaxSlots >= 32 && Q == 1) return pick_np<T, VEC, Q, 32, VCS, XS>(np); break;
   }
   return nullptr;
 }
 
-template <typename T, int VEC, bool VCS>
+template <typename T, int VEC, bool VCS, bool XS>
 KernelPtr<T, VCS> pick_q(int Q, int G, int np) {
   switch (Q) {
-    case 1: return pick_g<T, VEC, 1, VCS>(G, np);
-    case 2: return pick_g<T, VEC, 2, VCS>(G, np);
-    case 4: return pick_g<T, VEC, 4, VCS>(G, np);
+    case 1: return pick_g<T, VEC, 1, VCS, XS>(G, np);
+    case 2: return pick_g<T, VEC, 2, VCS, XS>(G, np);
+    case 4: return pick_g<T, VEC, 4, VCS, XS>(G, np);
   }
   return nullptr;
 }
 
+// Lane tiling of a launch of wb columns: 16-byte vectors when the operands
+// allow them, Q lanes per slot (one vector, or one element, each, up to 4),
+// TW = Q * VEC columns per pass.
+struct Tiling {
+  bool vec;
+  int Q, TW;
+};
+template <typename T>
+Tiling gather_tiling(int wb, const void *xp, const void *yp, int64_t ldx, int64_t ldy) {
+  constexpr int VW = 16 / sizeof(T);
+  const bool vec = wb % VW == 0 && reinterpret_cast<uintptr_t>(xp) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(yp) % 16 == 0 && ldx % VW == 0 && ldy % VW == 0;
+  const int ncol = vec ? wb / VW : wb;
+  const int Q = ncol >= 3 ? 4 : ncol;
+  return Tiling{vec, Q, Q * (vec ? VW : 1)};
+}
+
+// Shared memory per CTA beyond the pipeline that the X slab may take.
+constexpr int64_t kSmemOptIn = 227 * 1024;
 template <typename T, bool VCS>
+constexpr int64_t slab_budget() {
+  return kSmemOptIn - pipe_smem_bytes<T, VCS, GatherShape<true, VCS>::kStageBufs>(0);
+}
+
+// Whether X fits the shared-memory slab for at least one column pass.
+template <typename T, bool VCS>
+bool slab_fits(const Matrix &m, DenseView X, DenseView Y, int64_t w) {
+  const int wb = (int)std::min<int64_t>(kMaxBlockWidth, w);
+  const Tiling t = gather_tiling<T>(wb, X.p, Y.p, X.ld, Y.ld);
+  return m.n_minor > 0 && m.n_minor * t.TW * (int64_t)sizeof(T) <= slab_budget<T, VCS>();
+}
+
+template <typename T, bool VCS, bool XS>
 vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s) {
-  constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
-  constexpr int smem = pipe_smem_bytes<T, VCS>(0);
-  for (int64_t c0 = 0; c0 < w; c0 += kMaxBlockWidth) {
-    const int wb = (int)std::min<int64_t>(kMaxBlockWidth, w - c0);
+  constexpr int VW = 16 / sizeof(T);
+  using Shape = GatherShape<XS, VCS>;
+  if ((uint64_t)X.ld * sizeof(T) >= (uint64_t(1) << 32)) {  // row offsets are 32-bit products
+    set_error("dense operand row stride too large");
+    return VS_ERR_UNSUPPORTED;
+  }
+  for (int64_t c0 = 0; c0 < w;) {
+    int wb = (int)std::min<int64_t>(kMaxBlockWidth, w - c0);
     const T *xp = static_cast<const T *>(X.p) + c0;
     T *yp = static_cast<T *>(Y.p) + c0;
-    const bool vec = wb % VW == 0 && reinterpret_cast<uintptr_t>(xp) % 16 == 0 &&
-                     reinterpret_cast<uintptr_t>(yp) % 16 == 0 && X.ld % VW == 0 &&
-                     Y.ld % VW == 0;
-    // lanes per slot across the width: one 16-byte vector (or one element) each, up to 4
-    const int ncol = vec ? wb / VW : wb;
-    const int Q = ncol >= 3 ? 4 : ncol;  // 1, 2 or 4
-    const int G = std::min(std::min(m.g, kMaxSlots), 32 / Q);
+    const Tiling t = gather_tiling<T>(wb, xp, yp, X.ld, Y.ld);
+    int64_t slab = 0;
+    if constexpr (XS) {
+      const int64_t pass = m.n_minor * t.TW * (int64_t)sizeof(T);
+      const int64_t fit = slab_budget<T, VCS>() / pass;  // column passes the slab holds
+      if (fit < 1) {
+        set_error("dense operand does not fit the shared-memory slab");
+        return VS_ERR_UNSUPPORTED;
+      }
+      wb = (int)std::min<int64_t>(wb, fit * t.TW);
+      slab = (wb + t.TW - 1) / t.TW * pass;
+    }
+    const int G = std::min(std::min(m.g, kMaxSlots), 32 / t.Q);
     const int NP = m.g / G;
-    KernelPtr<T, VCS> k = vec ? pick_q<T, VW, VCS>(Q, G, NP) : pick_q<T, 1, VCS>(Q, G, NP);
+    KernelPtr<T, VCS> k = t.vec ? pick_q<T, VW, VCS, XS>(t.Q, G, NP)
+                                : pick_q<T, 1, VCS, XS>(t.Q, G, NP);
     if (!k) {
       set_error("no gather kernel for this width and group size");
       return VS_ERR_UNSUPPORTED;
     }
+    const int smem = pipe_smem_bytes<T, VCS, Shape::kStageBufs>((int)slab);
     GatherArgs a;
     a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
                        nullptr, 0, 0, 0};
@@ -308,16 +427,18 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     a.Y = yp;
     a.ldy = Y.ld;
     a.w = wb;
+    a.n_x = (int)m.n_minor;
     a.partials = m.partials;
     a.counters = m.counters;
     int per_sm = 0;
     VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kPipeThreads, smem));
+    VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, Shape::kThreads, smem));
     const int64_t grid = std::min<int64_t>(m.n_blocks, (int64_t)std::max(1, per_sm) * m.n_sm);
     if (grid > 0) {
-      k<<<(unsigned)grid, kPipeThreads, smem, s>>>(a);
+      k<<<(unsigned)grid, Shape::kThreads, smem, s>>>(a);
       VS_LAUNCH_CHECK();
     }
+    c0 += wb;
   }
   return VS_OK;
 }

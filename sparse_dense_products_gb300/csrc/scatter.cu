@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kPipeThreads) scatter_atomic_kernel(const Scat
   int i = 0, rot = 0;  // rot: units handed out so far, mod kWarpsPerCta
   for (int b = blockIdx.x; b < a.st.n_blocks; b += gridDim.x, ++i) {
     if (!pipe.acquire(i, a.st)) return;
-    const Block k = load_block(a.st.blocks, b);
+    const Block k = stage_desc<T, VCS>(pipe.buf(i % kStages));
     const Staged<T, VCS> sv = stage_views<T, VCS>(k, pipe.buf(i % kStages));
     const int units = block_units(k, a.S);
     T x[CI][VEC];
@@ -217,8 +217,8 @@ __device__ __forceinline__ bool two_phase_prepare(const Pipe<T, VCS> &pipe, cons
   if (!mbar_wait_bounded(pipe.full(s), (j / kStages) & 1, kWaitLimitNs)) return false;
   const int lane = threadIdx.x & 31;
   const unsigned lt = lanemask_lt(), le = lt | (1u << lane);
-  const Block k = load_block(a.blocks, b);
   unsigned char *bp = pipe.buf(s);
+  const Block k = stage_desc<T, VCS>(bp);
   const Staged<T, VCS> sv = stage_views<T, VCS>(k, bp);
   const float *rv = VCS ? reinterpret_cast<const float *>(bp + LY::kRvals) - align_down<4>(k.r0)
                         : nullptr;
@@ -437,13 +437,16 @@ __global__ void __launch_bounds__(kPipeThreads) two_phase_kernel(const TwoPhaseA
     const bool search = VCS && a.sorted && rows < a.n_t;
     int i = 0, done = 0;
     bool ok = true;
+    DescWindow win;
     for (int b = b_lo; b < b_hi; ++b, ++i) {
       const int st = i % kStages;
       if (i >= kStages && !mbar_wait_bounded(pipe.empty(st), ((i / kStages) - 1) & 1, kWaitLimitNs)) {
         ok = false;
         break;
       }
-      if (lane == 0) stage_issue<T, VCS>(a.st, b, pipe.buf(st), pipe.full(st));
+      int4 d[3];
+      win.get(a.st.blocks, b_lo, 1, b_hi, i, d);
+      if (lane == 0) stage_issue<T, VCS>(a.st, d, pipe.buf(st), pipe.full(st));
       __syncwarp();
       for (; done < i; ++done)
         if (!two_phase_prepare<T, VCS>(pipe, a.st, done, b_lo + done, recs, prep, t0, rows, search)) {
@@ -481,7 +484,7 @@ __global__ void __launch_bounds__(kPipeThreads) two_phase_kernel(const TwoPhaseA
         pipe.give_up(a.st);
         break;
       }
-      const Block k = load_block(a.st.blocks, b);
+      const Block k = stage_desc<T, VCS>(pipe.buf(st));
       const unsigned char *rb = recs + st * RL::kBytes;
       if (lo < hi)
         WP::run(reinterpret_cast<const uint32_t *>(rb + RL::kKey),

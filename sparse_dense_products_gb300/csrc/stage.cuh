@@ -11,7 +11,8 @@
 // Each CTA runs a producer/consumer pipeline over its blocks.  One producer
 // warp brings a block's index, value, slice-pointer and run arrays into one of
 // kStages shared-memory buffers with bulk copies (cp.async.bulk), signalled on
-// the buffer's "full" mbarrier; the kWarpsPerCta consumer warps take work
+// the buffer's "full" mbarrier; the consumer warps (kWarpsPerCta, or the
+// count the kernel passes to Pipe::init) take work
 // units of the block (groups of slices, or shares) from a per-buffer counter
 // and, when the block has no work left, arrive on its "empty" mbarrier, which
 // lets the producer refill the buffer.  Warps never wait for one another
@@ -59,28 +60,33 @@ struct StageLayout {
   static constexpr int kRvals = kVptr + (VCS ? kCapRuns * 4 : 0);                   // VCS only
   static constexpr int kEvals = kRvals + (VCS ? kCapRuns * 4 : 0);                  // VCS only
   static constexpr int kBitmap = kEvals + (VCS ? kCapEntries * 4 : 0);              // VCS only
-  static constexpr int kBytes = kBitmap + (VCS ? ((kCapEntries + 31) / 32 * 4 + 15) / 16 * 16 : 0);
+  static constexpr int kWords = (kCapEntries + 31) / 32;                           // bitmap words
+  static constexpr int kBases = kBitmap + (VCS ? (kWords * 4 + 15) / 16 * 16 : 0);  // VCS only
+  static constexpr int kDesc = kBases + (VCS ? (kWords * 4 + 15) / 16 * 16 : 0);
+  static constexpr int kBytes = kDesc + 3 * 16;  // the block's descriptor, copied by the producer
   static_assert(kVals % 16 == 0 && kPtr % 16 == 0 && kVptr % 16 == 0 && kRvals % 16 == 0 &&
-                    kEvals % 16 == 0 && kBitmap % 16 == 0 && kBytes % 16 == 0,
+                    kEvals % 16 == 0 && kBitmap % 16 == 0 && kBases % 16 == 0 && kDesc % 16 == 0 &&
+                    kBytes % 16 == 0,
                 "stage arrays must start on 16-byte boundaries");
 };
 
-// Shared memory of a pipelined kernel: the stage buffers, then the control
-// words (full and empty barriers, work counters, failure flag), then `extra`.
-template <typename T, bool VCS>
+// Shared memory of a pipelined kernel with NS stage buffers: the buffers,
+// then the control words (full and empty barriers, work counters, failure
+// flag), then `extra`.
+template <typename T, bool VCS, int NS = kStages>
 struct PipeLayout {
   static constexpr int kBufs = 0;
-  static constexpr int kFull = kStages * StageLayout<T, VCS>::kBytes;
-  static constexpr int kEmpty = kFull + 8 * kStages;
-  static constexpr int kReady = kEmpty + 8 * kStages;  // VCS: run values expanded
-  static constexpr int kCounter = kReady + 8 * kStages;
-  static constexpr int kFail = kCounter + 4 * kStages;
+  static constexpr int kFull = NS * StageLayout<T, VCS>::kBytes;
+  static constexpr int kEmpty = kFull + 8 * NS;
+  static constexpr int kReady = kEmpty + 8 * NS;  // VCS: run values expanded
+  static constexpr int kCounter = kReady + 8 * NS;
+  static constexpr int kFail = kCounter + 4 * NS;
   static constexpr int kExtra = (kFail + 4 + 127) / 128 * 128;
 };
 
-template <typename T, bool VCS>
+template <typename T, bool VCS, int NS = kStages>
 constexpr int pipe_smem_bytes(int extra) {
-  return PipeLayout<T, VCS>::kExtra + extra;
+  return PipeLayout<T, VCS, NS>::kExtra + extra;
 }
 
 // A block's descriptor, decoded.
@@ -91,10 +97,48 @@ struct Block {
   int sfirst, nsh;        // chunk blocks: first share of the slice, shares of the slice
 };
 
-__device__ __forceinline__ Block load_block(const int4 *blocks, int b) {
-  const int4 x = blocks[3 * b], y = blocks[3 * b + 1], z = blocks[3 * b + 2];
+__device__ __forceinline__ Block decode_block(const int4 x, const int4 y, const int4 z) {
   return Block{x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w, z.x, z.y, z.z};
 }
+
+__device__ __forceinline__ Block load_block(const int4 *blocks, int b) {
+  return decode_block(blocks[3 * b], blocks[3 * b + 1], blocks[3 * b + 2]);
+}
+
+// The descriptor of the block held by a stage buffer (written at issue).
+template <typename T, bool VCS>
+__device__ __forceinline__ Block stage_desc(const unsigned char *buf) {
+  const int4 *d = reinterpret_cast<const int4 *>(buf + StageLayout<T, VCS>::kDesc);
+  return decode_block(d[0], d[1], d[2]);
+}
+
+// A producer warp's window of 32 block descriptors, one per lane, so that the
+// global loads of descriptors are not on the issue path of every block.
+struct DescWindow {
+  int4 x, y, z;
+  int first = -1;  // position (in the warp's block sequence) of lane 0's block
+  // Descriptor of the i-th block of the sequence b_begin + i * step (all lanes).
+  __device__ __forceinline__ void get(const int4 *blocks, int b_begin, int step, int b_end, int i,
+                                      int4 (&d)[3]) {
+    const int lane = threadIdx.x & 31;
+    if (first < 0 || i >= first + 32) {
+      first = i - i % 32;
+      const int b = b_begin + (first + lane) * step;
+      if (b < b_end) {
+        x = blocks[3 * b];
+        y = blocks[3 * b + 1];
+        z = blocks[3 * b + 2];
+      }
+    }
+    const int src = i - first;
+    d[0] = make_int4(__shfl_sync(kFullMask, x.x, src), __shfl_sync(kFullMask, x.y, src),
+                     __shfl_sync(kFullMask, x.z, src), __shfl_sync(kFullMask, x.w, src));
+    d[1] = make_int4(__shfl_sync(kFullMask, y.x, src), __shfl_sync(kFullMask, y.y, src),
+                     __shfl_sync(kFullMask, y.z, src), __shfl_sync(kFullMask, y.w, src));
+    d[2] = make_int4(__shfl_sync(kFullMask, z.x, src), __shfl_sync(kFullMask, z.y, src),
+                     __shfl_sync(kFullMask, z.z, src), __shfl_sync(kFullMask, z.w, src));
+  }
+};
 
 // Work units of a block: groups of S slices, or shares of a chunk.
 __device__ __forceinline__ int block_units(const Block &k, int S) {
@@ -129,13 +173,18 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// Producer: issue the bulk copies of block `b` into `buf` and arm `bar`.
+// Producer (one thread): copy the descriptor d of a block into `buf`, issue
+// the bulk copies of the block's arrays and arm `bar`.
 template <typename T, bool VCS>
-__device__ __forceinline__ void stage_issue(const StageArrays &a, int b, unsigned char *buf,
-                                            uint64_t *bar) {
+__device__ __forceinline__ void stage_issue(const StageArrays &a, const int4 (&d)[3],
+                                            unsigned char *buf, uint64_t *bar) {
   using LY = StageLayout<T, VCS>;
   constexpr int VPE = 16 / (int)sizeof(T);  // values per 16 bytes
-  const Block k = load_block(a.blocks, b);
+  int4 *dst = reinterpret_cast<int4 *>(buf + LY::kDesc);
+  dst[0] = d[0];
+  dst[1] = d[1];
+  dst[2] = d[2];
+  const Block k = decode_block(d[0], d[1], d[2]);
   uint32_t bytes = 0;
   int n_idx = 0, n_val = 0, n_ptr = 0, n_vp = 0, n_rv = 0;
   const int ei = align_down<4>(k.e0);
@@ -180,6 +229,14 @@ __device__ __forceinline__ void stage_issue(const StageArrays &a, int b, unsigne
   }
 }
 
+// Same, loading the descriptor of block number b from global memory.
+template <typename T, bool VCS>
+__device__ __forceinline__ void stage_issue(const StageArrays &a, int b, unsigned char *buf,
+                                            uint64_t *bar) {
+  const int4 d[3] = {a.blocks[3 * b], a.blocks[3 * b + 1], a.blocks[3 * b + 2]};
+  stage_issue<T, VCS>(a, d, buf, bar);
+}
+
 template <typename T, bool VCS>
 __device__ __forceinline__ Staged<T, VCS> stage_views(const Block &k, unsigned char *buf) {
   using LY = StageLayout<T, VCS>;
@@ -221,9 +278,9 @@ __device__ __forceinline__ void expand_runs(const Block &k, unsigned char *buf, 
 }
 
 // The pipeline's shared-memory control words.
-template <typename T, bool VCS>
+template <typename T, bool VCS, int NS = kStages>
 struct Pipe {
-  using PL = PipeLayout<T, VCS>;
+  using PL = PipeLayout<T, VCS, NS>;
   unsigned char *smem;
   __device__ __forceinline__ unsigned char *buf(int s) const {
     return smem + PL::kBufs + s * StageLayout<T, VCS>::kBytes;
@@ -242,12 +299,13 @@ struct Pipe {
   }
   __device__ __forceinline__ int *fail() const { return reinterpret_cast<int *>(smem + PL::kFail); }
 
-  // All threads; contains __syncthreads.
-  __device__ __forceinline__ void init() const {
+  // All threads; contains __syncthreads.  `consumers`: warps that release
+  // each buffer.
+  __device__ __forceinline__ void init(int consumers = kWarpsPerCta) const {
     if (threadIdx.x == 0) {
-      for (int s = 0; s < kStages; ++s) {
+      for (int s = 0; s < NS; ++s) {
         mbar_init(full(s), 1);
-        mbar_init(empty(s), kWarpsPerCta);
+        mbar_init(empty(s), consumers);
         mbar_init(ready(s), 1);
       }
       *fail() = 0;
@@ -263,23 +321,24 @@ struct Pipe {
     }
   }
 
-  // VCS, producer warp: once block j (number b) has landed, write the run
-  // value of each of its entries into the per-entry value array and mark the
-  // stage ready.  Run starts go into a bitmap over the block's entries; the
-  // run of entry n is then r0 - 1 + (run starts in [e0, n]), counted with
-  // popcounts 32 entries at a time.
-  __device__ __forceinline__ bool expand(const StageArrays &a, int j, int b) const {
+  // VCS, producer warp: block j (number b) has landed; write the run value of
+  // each of its entries into the per-entry value array and mark the stage
+  // ready.  Run starts go into a bitmap over the block's entries; the run of
+  // entry n is then r0 - 1 + (run starts in [e0, n]).  A warp scan of the
+  // words' popcounts gives each word the runs started before it; the words
+  // are then independent, so the final pass has no chain between words.
+  __device__ __forceinline__ void expand(const StageArrays &a, int j, int b) const {
     using LY = StageLayout<T, VCS>;
-    const int s = j % kStages;
-    if (!mbar_wait_bounded(full(s), (j / kStages) & 1, kWaitLimitNs)) return false;
+    const int s = j % NS;
     const int lane = threadIdx.x & 31;
-    const Block k = load_block(a.blocks, b);
     unsigned char *bp = buf(s);
+    const Block k = stage_desc<T, VCS>(bp);
     const int eb = align_down<4>(k.e0);
     const int32_t *vp = reinterpret_cast<const int32_t *>(bp + LY::kVptr) - align_down<4>(k.r0);
     const float *rv = reinterpret_cast<const float *>(bp + LY::kRvals) - align_down<4>(k.r0);
     float *ev = reinterpret_cast<float *>(bp + LY::kEvals) - eb;
     uint32_t *bm = reinterpret_cast<uint32_t *>(bp + LY::kBitmap);
+    int *wb = reinterpret_cast<int *>(bp + LY::kBases);
     const int nwords = (k.e1 - eb + 31) / 32;
     for (int q = lane; q < nwords; q += 32) bm[q] = 0u;
     __syncwarp();
@@ -288,69 +347,159 @@ struct Pipe {
       atomicOr(&bm[st >> 5], 1u << (st & 31));
     }
     __syncwarp();
+    int base = k.r0 - 1;  // runs started before word q0
+    for (int q0 = 0; q0 < nwords; q0 += 32) {
+      const bool has = q0 + lane < nwords;
+      const int c = has ? __popc(bm[q0 + lane]) : 0;
+      int incl = c;  // inclusive scan of the popcounts over the lanes
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, incl, d);
+        if (lane >= d) incl += y;
+      }
+      if (has) wb[q0 + lane] = base + incl - c;
+      base += __shfl_sync(kFullMask, incl, 31);
+    }
+    __syncwarp();
     const unsigned le = lanemask_lt() | (1u << lane);
-    int run = k.r0 - 1;
+#pragma unroll 8
     for (int q = 0; q < nwords; ++q) {
-      const uint32_t word = bm[q];
       const int n = eb + 32 * q + lane;
-      if (n >= k.e0 && n < k.e1) ev[n] = rv[run + __popc(word & le)];
-      run += __popc(word);
+      if (n >= k.e0 && n < k.e1) ev[n] = rv[wb[q] + __popc(bm[q] & le)];
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(ready(s));
-    return true;
   }
 
   // Producer warp (all lanes; lane 0 issues): fills the ring with blocks
-  // b_begin, b_begin + step, ... < b_end, each after the consumers released
-  // its buffer; for VCS it also expands each landed block's run values, one
-  // block behind the newest copy.  Before returning, waits
-  // (bounded) until every issued copy has landed.
+  // b_begin, b_begin + step, ... < b_end, each once the consumers released
+  // its buffer.  For VCS the warp also expands each block's run values as
+  // soon as the block has landed: it polls both conditions, issuing first,
+  // so copies stay in flight while it expands.  Every wait is bounded; before
+  // returning it waits (bounded) until every issued copy has landed.
   __device__ __forceinline__ void produce(const StageArrays &a, int b_begin, int b_end,
                                           int step) const {
     const int lane = threadIdx.x & 31;
-    int i = 0, done = 0;  // blocks issued, blocks expanded
+    const int total = b_end > b_begin ? (b_end - b_begin + step - 1) / step : 0;
+    int issued = 0, done = 0;  // blocks issued, blocks expanded (VCS)
     bool ok = true;
-    for (int b = b_begin; b < b_end; b += step, ++i) {
-      const int s = i % kStages;
-      if (i >= kStages && !mbar_wait_bounded(empty(s), ((i / kStages) - 1) & 1, kWaitLimitNs)) {
-        ok = false;
-        break;
-      }
-      if (*reinterpret_cast<volatile int *>(fail())) {
-        ok = false;
-        break;
-      }
+    DescWindow win;
+    auto issue = [&](int i) {
+      int4 d[3];
+      win.get(a.blocks, b_begin, step, b_end, i, d);
       if (lane == 0) {
-        *counter(s) = 0;
-        stage_issue<T, VCS>(a, b, buf(s), full(s));
+        *counter(i % NS) = 0;
+        stage_issue<T, VCS>(a, d, buf(i % NS), full(i % NS));
       }
       __syncwarp();
-      // expand the previous block now (it was issued one round ago), so the
-      // consumers find kStages - 2 expanded blocks ahead of them
-      for (; VCS && done < i; ++done)
-        if (!expand(a, done, b_begin + done * step)) {
+    };
+    if constexpr (!VCS) {
+      for (; issued < total; ++issued) {
+        const int s = issued % NS;
+        if ((issued >= NS && !mbar_wait_bounded(empty(s), ((issued / NS) - 1) & 1, kWaitLimitNs)) ||
+            *reinterpret_cast<volatile int *>(fail())) {
           ok = false;
           break;
         }
-      if (!ok) break;
+        issue(issued);
+      }
+    } else {
+      int idle = 0;
+      uint64_t t0 = 0;
+      while (done < total) {
+        bool moved = false;
+        if (issued < total) {
+          const int s = issued % NS;
+          bool freed = issued < NS || mbar_test(empty(s), ((issued / NS) - 1) & 1);
+          freed = __shfl_sync(kFullMask, freed, 0);
+          if (freed) {
+            issue(issued++);
+            moved = true;
+          }
+        }
+        if (done < issued) {
+          bool landed = mbar_test(full(done % NS), (done / NS) & 1);
+          landed = __shfl_sync(kFullMask, landed, 0);
+          if (landed) {
+            expand(a, done, b_begin + done * step);
+            ++done;
+            moved = true;
+          }
+        }
+        if (moved) {
+          idle = 0;
+          continue;
+        }
+        if (idle++ == 0) t0 = global_ns();
+        if ((idle & 63) == 0) {
+          bool stop = *reinterpret_cast<volatile int *>(fail()) != 0 ||
+                      global_ns() - t0 > kWaitLimitNs;
+          stop = __shfl_sync(kFullMask, stop, 0);
+          if (stop) {
+            ok = false;
+            break;
+          }
+        }
+      }
     }
-    if (VCS && ok)
-      for (; done < i; ++done)
-        if (!expand(a, done, b_begin + done * step)) {
-          ok = false;
-          break;
-        }
     if (!ok) give_up(a);
     if (lane == 0)
-      for (int j = i - kStages < 0 ? 0 : i - kStages; j < i; ++j)
-        mbar_wait_bounded(full(j % kStages), (j / kStages) & 1, kWaitLimitNs);
+      for (int j = issued - NS < 0 ? 0 : issued - NS; j < issued; ++j)
+        mbar_wait_bounded(full(j % NS), (j / NS) & 1, kWaitLimitNs);
+  }
+
+  // Split producer, issuing warp: issues every block in order, each once the
+  // consumers released its buffer; before returning waits (bounded) until
+  // every issued copy has landed.  The VCS run values are left to
+  // expand_share.
+  __device__ __forceinline__ void issue_all(const StageArrays &a, int b_begin, int b_end,
+                                            int step) const {
+    const int lane = threadIdx.x & 31;
+    const int total = b_end > b_begin ? (b_end - b_begin + step - 1) / step : 0;
+    DescWindow win;
+    int issued = 0;
+    bool ok = true;
+    for (; issued < total; ++issued) {
+      const int s = issued % NS;
+      if ((issued >= NS && !mbar_wait_bounded(empty(s), ((issued / NS) - 1) & 1, kWaitLimitNs)) ||
+          *reinterpret_cast<volatile int *>(fail())) {
+        ok = false;
+        break;
+      }
+      int4 d[3];
+      win.get(a.blocks, b_begin, step, b_end, issued, d);
+      if (lane == 0) {
+        *counter(s) = 0;
+        stage_issue<T, VCS>(a, d, buf(s), full(s));
+      }
+      __syncwarp();
+    }
+    if (!ok) give_up(a);
+    if (lane == 0)
+      for (int j = issued - NS < 0 ? 0 : issued - NS; j < issued; ++j)
+        mbar_wait_bounded(full(j % NS), (j / NS) & 1, kWaitLimitNs);
+  }
+
+  // Split producer, expanding warp e of E (E divides NS, so the blocks of a
+  // buffer always come to the same warp, in order, and a parity wait can never
+  // see an older phase): expands blocks e, e + E, ... as they land.
+  __device__ __forceinline__ void expand_share(const StageArrays &a, int b_begin, int b_end,
+                                               int step, int e, int E) const {
+    const int total = b_end > b_begin ? (b_end - b_begin + step - 1) / step : 0;
+    for (int i = e; i < total; i += E) {
+      if (!mbar_wait_bounded(full(i % NS), (i / NS) & 1, kWaitLimitNs) ||
+          *reinterpret_cast<volatile int *>(fail())) {
+        give_up(a);
+        return;
+      }
+      expand(a, i, b_begin + i * step);
+    }
   }
 
   // Consumer warp: waits for the i-th block of this CTA; false if the wait gave up.
   __device__ __forceinline__ bool acquire(int i, const StageArrays &a) const {
-    uint64_t *bar = VCS ? ready(i % kStages) : full(i % kStages);
-    if (mbar_wait_bounded(bar, (i / kStages) & 1, kWaitLimitNs)) return true;
+    uint64_t *bar = VCS ? ready(i % NS) : full(i % NS);
+    if (mbar_wait_bounded(bar, (i / NS) & 1, kWaitLimitNs)) return true;
     give_up(a);
     return false;
   }
@@ -358,13 +507,13 @@ struct Pipe {
   // Consumer warp: done with the i-th block.
   __device__ __forceinline__ void release(int i) const {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(empty(i % kStages));
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty(i % NS));
   }
 
   // Consumer warp: next work unit of the i-th block (warp-uniform).
   __device__ __forceinline__ int grab(int i) const {
     int u = 0;
-    if ((threadIdx.x & 31) == 0) u = atomicAdd(counter(i % kStages), 1);
+    if ((threadIdx.x & 31) == 0) u = atomicAdd(counter(i % NS), 1);
     return __shfl_sync(kFullMask, u, 0);
   }
 };

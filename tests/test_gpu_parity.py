@@ -247,6 +247,33 @@ def test_repeats_bit_identical_and_column_alone_equals_batch(layout, major, dire
             assert torch.equal(alone.reshape(-1), col.reshape(-1)), (variant, c)
 
 
+def _columns(B, direction, c0, c1):
+    """Columns [c0, c1) of the dense operand as a new operand of the same layout."""
+    if direction == "A@B":
+        return B[:, c0:c1].contiguous()
+    return B[c0:c1, :].t().contiguous().t()
+
+
+@pytest.mark.parametrize("layout", ["csr", "vcs"])
+@pytest.mark.parametrize("major,direction", [("row", "A@B"), ("col", "B@A")])
+def test_shared_slab_and_l1_gathers_agree_bitwise(layout, major, direction):
+    """X of 6,000 rows: widths 1 and 4 keep it in a shared-memory slab, width 16
+    reads it through L1.  The summation tree is fixed by the matrix, so every
+    column has the same bits either way."""
+    shape = (3000, 6000) if major == "row" else (6000, 3000)
+    coo = W.random_coo(*shape, 600_000, seed=31, values="counts", sort=False)
+    A = build(coo, layout, major)
+    B, Bt = dense_operand(coo, direction, 16, torch.float32, seed=3)
+    batch = _run(A, B, direction, "deterministic")
+    want, D = oracle_product(coo, oracle_triples(coo, layout, major), direction, Bt)
+    assert_close(gpu_out_rows(batch, direction), want, D, 1e-5, f"{layout}/{major} w=16")
+    for c0, c1 in ((0, 1), (7, 8), (15, 16), (4, 8), (12, 16)):
+        part = _run(A, _columns(B, direction, c0, c1), direction, "deterministic")
+        ref = batch[:, c0:c1] if direction == "A@B" else batch[c0:c1, :]
+        assert torch.equal(part, ref), (c0, c1)
+    A.destroy()
+
+
 def test_atomic_and_deterministic_agree_within_tolerance_on_main_workload():
     coo = workload("main")
     for layout, major, direction in [("vcs", "col", "A@B"), ("vcs", "row", "B@A"),
