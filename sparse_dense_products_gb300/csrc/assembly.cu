@@ -638,6 +638,7 @@ vs_status prepare_matrix(Matrix &m, cudaStream_t s) {
     desc.push_back(z);
   };
   int64_t n_long = 0, n_chunks = 0, n_shares = 0;
+  std::vector<int4> longs;  // {slice, first share, shares, 0} per long slice
   int64_t bs0 = -1, be = 0, br = 0;  // open slice block: first slice, entries, runs
   auto close_slices = [&](int64_t s_end) {
     if (bs0 < 0) return;
@@ -692,6 +693,7 @@ vs_status prepare_matrix(Matrix &m, cudaStream_t s) {
       sh += (ch[k2].y - ch[k2].x + kShareEntries - 1) / kShareEntries;
     }
     n_chunks += (int64_t)ch.size();
+    longs.push_back(make_int4((int)sl, (int)n_shares, (int)slice_shares, 0));
     n_shares += slice_shares;
     ++n_long;
   }
@@ -706,8 +708,8 @@ vs_status prepare_matrix(Matrix &m, cudaStream_t s) {
                             cudaMemcpyHostToDevice, s));
   }
   if (n_long > 0) {
-    VS_TRY(dev_alloc((void **)&m.counters, sizeof(int) * n_long));
-    VS_CUDA(cudaMemsetAsync(m.counters, 0, sizeof(int) * n_long, s));
+    VS_TRY(dev_alloc((void **)&m.longs, sizeof(int4) * n_long));
+    VS_CUDA(cudaMemcpyAsync(m.longs, longs.data(), sizeof(int4) * n_long, cudaMemcpyHostToDevice, s));
     VS_TRY(dev_alloc(&m.partials, m.dsize() * kMaxBlockWidth * n_shares));
   }
   VS_TRY(dev_alloc((void **)&m.err, sizeof(int)));

@@ -21,19 +21,22 @@
 //     meet in the butterfly p[k] += p[k + h], h = g/2, ..., 1;
 //   * a long slice is cut into chunks (at most kBlockEntries entries and
 //     kBlockRuns runs, cut points fixed by the matrix) and every chunk into
-//     shares of kShareEntries entries; the share results are added in share
-//     order ((p0 + p1) + p2) + ... by the last share of the slice to finish.
+//     shares of kShareEntries entries; share_combine_kernel adds the m share
+//     results of the slice: lane l of a warp sums shares l, l + 32, ... in
+//     order, then the 32 lane sums meet in a butterfly.
 // Physically G slots of a slice each hold NP = g / G partials in registers
 // (Q lanes per slot across a tile of Q * VEC columns; wider products take
 // several column passes over the same staged entries; narrow ones put several
-// slices in one warp).  In-lane adds, then
-// shuffles, reproduce the same tree for every width, so bits never depend on w.
+// slices in one warp).  In-lane adds, then shuffles, reproduce the same tree
+// for every width, so bits never depend on w, nor on where X is read from.
 //
-// Data movement: entries, values, slice pointers and runs arrive in shared
-// memory by bulk copies through a 4-deep ring fed by a producer warp
-// (stage.cuh); the producer warp also expands VCS run values to per-entry
-// values in shared memory; the dense rows X[t, :] are gathered through L1 with
-// 16-byte vector loads.
+// Data movement: entries, values, slice pointers, runs and the block's
+// descriptor arrive in shared memory by bulk copies through a ring of stage
+// buffers fed by a producer warp (stage.cuh); VCS run values are expanded to
+// per-entry values in shared memory by the producer side.  The dense rows
+// X[t, :] come either from a shared-memory slab holding all of X (when it
+// fits: one CTA per SM copies it in once) or through L1 with 16-byte vector
+// loads.
 #pragma once
 
 #include <algorithm>
@@ -56,14 +59,7 @@ struct GatherArgs {
   int w;           // columns in this launch (<= kMaxBlockWidth)
   int n_x;         // rows of X (shared-memory variant: rows copied into the slab)
   void *partials;  // [n_shares][kMaxBlockWidth] of T
-  int *counters;   // [n_long]
 };
-
-__device__ __forceinline__ int atomic_add_release(int *p, int v) {
-  int old;
-  asm volatile("atom.add.release.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
 
 // Where the rows X[t, :] come from.  Each lane holds the address of its own
 // VEC columns in row 0 (a valid column even for lanes past the width, whose
@@ -172,19 +168,21 @@ __device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const XSr
       acc[0][e] = acc[0][e] + __shfl_xor_sync(kFullMask, acc[0][e], sft * Q);
 }
 
-// Launch shape: XS = false gathers X through L1 (8 consumer warps, 4 stage
-// buffers, 3 CTAs per SM, one producer warp); XS = true keeps X in shared
-// memory (16 consumer warps, 8 stage buffers, one CTA per SM, the slab taking
-// the rest of the SM's shared memory).  With one CTA per SM a single warp
-// cannot keep up with expanding VCS run values, so XS with VCS splits the
-// producer into one issuing warp and kExpanders expanding warps.
+// Launch shape.  XS = true keeps X in shared memory: 16 consumer warps, 8
+// stage buffers, one CTA per SM, the slab taking the rest of the SM's shared
+// memory.  XS = false gathers X through L1: CSR runs 3 CTAs per SM of 8
+// consumer warps and 4 stage buffers, each with one producer warp; VCS runs
+// one CTA per SM of 20 consumer warps and 8 stage buffers.  Expanding VCS run
+// values is a chain of shared-memory round trips that one warp per SM cannot
+// keep ahead of the consumers, so VCS splits the producer into one issuing
+// warp and kExpanders expanding warps.
 template <bool XS, bool VCS>
 struct GatherShape {
-  static constexpr int kWarps = XS ? 16 : kWarpsPerCta;
-  static constexpr int kStageBufs = XS ? 8 : kStages;
-  static constexpr int kExpanders = XS && VCS ? 4 : 0;
+  static constexpr int kWarps = XS ? 16 : (VCS ? 20 : kWarpsPerCta);
+  static constexpr int kStageBufs = XS || VCS ? 8 : kStages;
+  static constexpr int kExpanders = VCS ? 4 : 0;
   static constexpr int kThreads = (kWarps + 1 + kExpanders) * 32;
-  static constexpr int kMinCtas = XS ? 1 : VS_GATHER_MIN_CTAS;
+  static constexpr int kMinCtas = XS || VCS ? 1 : VS_GATHER_MIN_CTAS;
   static_assert(kExpanders == 0 || kStageBufs % kExpanders == 0,
                 "each stage buffer must always go to the same expanding warp");
 };
@@ -277,8 +275,8 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
             *reinterpret_cast<V *>(Y + (int64_t)s * a.ldy + col) = Ops::pack(acc[0]);
         }
       } else {
-        // ---- share u of a chunk of a long slice: publish its partial; the last
-        // share of the slice to arrive adds all of them in share order
+        // ---- share u of a chunk of a long slice: its partial goes to the
+        // share table; share_combine_kernel adds the shares of each slice
         const int na = k.e0 + u * kShareEntries, nb = min(k.e1, na + kShareEntries);
         const int n0 = sub == 0 ? na : 0, n1 = sub == 0 ? nb : 0;
         for (int cp = 0; cp < npass * TW; cp += TW) {
@@ -288,24 +286,32 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
             *reinterpret_cast<V *>(P + (int64_t)(k.first + u) * kMaxBlockWidth + col) =
                 Ops::pack(acc[0]);
         }
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomic_add_release(a.counters + k.lid, 1) == k.nsh - 1;
-        last = __shfl_sync(kFullMask, last, 0);
-        if (last) {
-          __threadfence();
-          for (int c = lane; c < w; c += 32) {
-            T sum = __ldcg(P + (int64_t)k.sfirst * kMaxBlockWidth + c);
-            for (int q = 1; q < k.nsh; ++q)
-              sum = sum + __ldcg(P + (int64_t)(k.sfirst + q) * kMaxBlockWidth + c);
-            Y[(int64_t)k.s0 * a.ldy + c] = sum;
-          }
-          if (lane == 0) a.counters[k.lid] = 0;  // re-armed for the next launch
-        }
       }
     }
     pipe.release(i);
   }
+}
+
+// Y[s, c] of every long slice s from its share partials p_0 .. p_{m-1}: lane
+// l adds p_l, p_{l+32}, ... in order (from zero), then the lanes meet in the
+// butterfly over strides 16, 8, 4, 2, 1.  One warp per (long slice, column);
+// the order depends on the share count alone.
+template <typename T>
+__global__ void __launch_bounds__(256) share_combine_kernel(const T *__restrict__ P,
+                                                            const int4 *__restrict__ longs,
+                                                            int64_t n_long, int w,
+                                                            T *__restrict__ Y, int64_t ldy) {
+  const int lane = threadIdx.x & 31;
+  const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (item >= n_long * w) return;
+  const int64_t l = item / w;
+  const int c = (int)(item - l * w);
+  const int4 d = longs[l];  // {slice, first share, shares, 0}
+  T sum = T(0);
+  for (int q = lane; q < d.z; q += 32) sum = sum + P[(int64_t)(d.y + q) * kMaxBlockWidth + c];
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) sum = sum + __shfl_xor_sync(kFullMask, sum, off);
+  if (lane == 0) Y[(int64_t)d.x * ldy + c] = sum;
 }
 
 // ------------------------------------------------------------------ dispatch
@@ -429,13 +435,18 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     a.w = wb;
     a.n_x = (int)m.n_minor;
     a.partials = m.partials;
-    a.counters = m.counters;
     int per_sm = 0;
     VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, Shape::kThreads, smem));
     const int64_t grid = std::min<int64_t>(m.n_blocks, (int64_t)std::max(1, per_sm) * m.n_sm);
     if (grid > 0) {
       k<<<(unsigned)grid, Shape::kThreads, smem, s>>>(a);
+      VS_LAUNCH_CHECK();
+    }
+    if (m.n_long > 0) {
+      const int64_t warps = m.n_long * wb;
+      share_combine_kernel<T><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
+          static_cast<const T *>(m.partials), m.longs, m.n_long, wb, yp, Y.ld);
       VS_LAUNCH_CHECK();
     }
     c0 += wb;

@@ -48,18 +48,19 @@ int64_t Matrix::layout_bytes() const {
 }
 
 int64_t Matrix::meta_bytes() const {
-  return (int64_t)sizeof(int4) * 3 * n_blocks + (int64_t)sizeof(int) * (n_long + 1) +
+  return (int64_t)sizeof(int4) * 3 * n_blocks + (int64_t)sizeof(int4) * n_long + (int64_t)sizeof(int) +
          (int64_t)dsize() * kMaxBlockWidth * n_shares + (int64_t)sizeof(int32_t) * (tp_chunks + 1);
 }
 
 void free_matrix(Matrix &m) {
   for (void *p : {(void *)m.ptr, (void *)m.idx, m.vals, (void *)m.vptr, (void *)m.blocks,
-                  (void *)m.counters, m.partials, (void *)m.tp_bounds, (void *)m.err})
+                  (void *)m.longs, m.partials, (void *)m.tp_bounds, (void *)m.err})
     if (p) cudaFree(p);
   m.ptr = m.idx = m.vptr = m.tp_bounds = nullptr;
   m.vals = m.partials = nullptr;
   m.blocks = nullptr;
-  m.counters = m.err = nullptr;
+  m.longs = nullptr;
+  m.err = nullptr;
 }
 
 vs_status Scratch::reserve(size_t need, cudaStream_t s) {

@@ -83,7 +83,7 @@ struct Matrix {
   int64_t n_long = 0;           // long slices
   int64_t n_chunks = 0;         // chunks over all long slices
   int64_t n_shares = 0;         // shares over all long slices
-  int *counters = nullptr;      // [n_long] arrival counters (always left at 0)
+  int4 *longs = nullptr;        // [n_long] {slice, first share, shares, 0}
   void *partials = nullptr;     // [n_shares * kMaxBlockWidth] of dtype
   int *err = nullptr;           // device flag: a bounded wait gave up
   bool sorted_segments = false; // minor indices ascend inside every run / row
