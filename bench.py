@@ -14,7 +14,7 @@ Metric: effective HBM GB/s = algorithmic bytes / device time, where the
 algorithmic bytes of a product are every array of the stored layout, the dense
 operand read once and the output written once.  L2 is flushed (a 512 MiB
 write) before every timed product; CUDA events bracket each product on the
-launching stream.
+launching stream; a product's time is the median over the timed steps.
 
 ``--impl reference`` times the float64 CPU oracle on the same workload and
 metric (the deliberately slow reference; host cores).
@@ -119,6 +119,37 @@ class Clocks:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def source_digest() -> str:
+    """Digest of the CUDA sources, to tell whether recorded ncu counters are current."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_dense_products_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(product: str):
+    """DRAM bytes (read + write) of one launch of `product`'s kernel, from the ncu
+    record in profiles/dram_traffic.txt, or None when the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        rec = {}
+        with open(path) as f:
+            for ln in f:
+                ln = ln.split("#", 1)[0].split()
+                if len(ln) == 2:
+                    rec[ln[0]] = ln[1]
+        if rec.get("source_digest") != source_digest():
+            return None
+        return int(rec[product])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def algorithmic_bytes(A, n_x_rows: int, n_y_rows: int, w: int, es: int = 4) -> int:
@@ -326,7 +357,8 @@ def gpu_arm(args):
     launches = vs.kernel_launches() - launches0
     if ws > 1:
         dist.barrier()
-    ms_prod = {k: statistics.mean(v) for k, v in per.items()}
+    ms_prod = {k: statistics.median(v) for k, v in per.items()}
+    ms_mean = {k: statistics.mean(v) for k, v in per.items()}
     ms_step = sum(ms_prod.values())
     step_bytes = sum(nbytes.values())
     t_local = ms_step
@@ -353,6 +385,8 @@ def gpu_arm(args):
     # ---- in-run cuSPARSE reference: torch's CSR matmul on the index-sorted CSR
     # (CSR@B), and on the CSR of the exact transpose for B@CSR (Y^T = A^T B^T)
     cusparse = {}
+    import warnings
+    warnings.filterwarnings("ignore", message="Sparse CSR tensor support is in beta")
     try:
         a = handles[("csr", "row")].arrays()
         A_csr = torch.sparse_csr_tensor(a["ptr"], a["indices"], a["values"], (n_rows, n_cols))
@@ -367,6 +401,15 @@ def gpu_arm(args):
                               "ours_over_cusparse_time": round(ms_prod[name] / ms, 3)}
     except Exception as exc:  # reported, never fatal: it is a comparison, not the path
         cusparse = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
+
+    # ---- host cost of one asynchronous vs_spmm call (enqueue only)
+    torch.cuda.synchronize()
+    n_calls = 200
+    t0 = time.perf_counter()
+    for q in range(n_calls):
+        run(*PRODUCTS[q % len(PRODUCTS)])
+    host_us = (time.perf_counter() - t0) / n_calls * 1e6
+    torch.cuda.synchronize()
 
     # ---- e2e through vs_spmm_host with pinned host buffers
     Bab_h = Bab.cpu().pin_memory()
@@ -396,9 +439,12 @@ def gpu_arm(args):
     peak, peak_kind = _peaks()
     dom = max(ms_prod, key=ms_prod.get)
     achieved = nbytes[dom] / (ms_prod[dom] * 1e-3) / 1e9
-    products = {k: {"ms": round(ms_prod[k], 5), "GBs": round(nbytes[k] / ms_prod[k] / 1e6, 1),
+    products = {k: {"ms": round(ms_prod[k], 5), "ms_mean": round(ms_mean[k], 5),
+                    "GBs": round(nbytes[k] / ms_prod[k] / 1e6, 1),
                     "frac_of_8TBs": round(nbytes[k] / ms_prod[k] / 1e6 / NOMINAL_HBM_GBS, 4),
+                    "frac_of_measured": round(nbytes[k] / ms_prod[k] / 1e6 / peak, 4),
                     "bytes": nbytes[k]} for k in ms_prod}
+    traffic = recorded_traffic(dom)
 
     # ---- CPU baseline: the float64 oracle on host cores (rank 0, N=1 only)
     cpu = None
@@ -425,7 +471,9 @@ def gpu_arm(args):
         "frac_of_8TBs": round(value / ws / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None},
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "per": "one launch of the product's gather kernel (median of the timed reps)"},
+        "host_us_per_call": round(host_us, 2),
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
@@ -449,7 +497,7 @@ def gpu_arm(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,

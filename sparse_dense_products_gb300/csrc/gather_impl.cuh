@@ -22,7 +22,7 @@
 //   * a long slice is cut into chunks (at most kBlockEntries entries and
 //     kBlockRuns runs, cut points fixed by the matrix) and every chunk into
 //     shares of kShareEntries entries; share_combine_kernel adds the m share
-//     results of the slice: lane l of a warp sums shares l, l + 32, ... in
+//     results of the slice: lane j of a warp sums shares j, j + 32, ... in
 //     order, then the 32 lane sums meet in a butterfly.
 // Physically G slots of a slice each hold NP = g / G partials in registers
 // (Q lanes per slot across a tile of Q * VEC columns; wider products take
@@ -183,6 +183,11 @@ struct GatherShape {
   static constexpr int kExpanders = VCS ? 4 : 0;
   static constexpr int kThreads = (kWarps + 1 + kExpanders) * 32;
   static constexpr int kMinCtas = XS || VCS ? 1 : VS_GATHER_MIN_CTAS;
+  // Consumer groups: block i of a CTA goes to group i mod kGroups only, so a
+  // warp pays the per-block bookkeeping for 1 / kGroups of the blocks.  Each
+  // stage buffer always serves the same group (kGroups divides the stages).
+  static constexpr int kGroups = XS || VCS ? 2 : 1;
+  static_assert(kStageBufs % kGroups == 0 && kWarps % kGroups == 0, "uneven consumer groups");
   static_assert(kExpanders == 0 || kStageBufs % kExpanders == 0,
                 "each stage buffer must always go to the same expanding warp");
 };
@@ -199,7 +204,8 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
   constexpr int TW = Q * VEC;      // columns per pass
   extern __shared__ __align__(128) unsigned char smem[];
   const Pipe<T, VCS, NS> pipe{smem};
-  pipe.init(NW);
+  constexpr int GW = NW / Shape::kGroups;  // consumer warps per group
+  pipe.init(GW);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (wid >= NW) {  // the producer warp(s)
     if constexpr (Shape::kExpanders == 0)
@@ -246,8 +252,10 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
     }
   };
 
-  int i = 0, rot = 0;  // rot: units handed out so far, mod NW
-  for (int b = blockIdx.x; b < a.st.n_blocks; b += gridDim.x, ++i) {
+  const int gw = wid % GW;  // this warp's place in its group
+  int i = wid / GW, rot = 0;  // rot: units the group handed out so far, mod GW
+  for (int b = blockIdx.x + i * gridDim.x; b < a.st.n_blocks;
+       b += Shape::kGroups * gridDim.x, i += Shape::kGroups) {
     if (!pipe.acquire(i, a.st)) return;
     unsigned char *buf = pipe.buf(i % NS);
     const Block k = stage_desc<T, VCS>(buf);
@@ -255,9 +263,9 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
     const int units = block_units(k, S);
     T acc[NP][VEC];
     // work units go round-robin to the consumer warps, continuing across blocks
-    const int u0 = (wid - rot + NW) % NW;
-    rot = (rot + units) % NW;
-    for (int u = u0; u < units; u += NW) {
+    const int u0 = (gw - rot + GW) % GW;
+    rot = (rot + units) % GW;
+    for (int u = u0; u < units; u += GW) {
       if (k.type == 0) {
         // ---- S consecutive slices, one per sub-group
         const int sa = k.s0 + u * S;
@@ -292,26 +300,64 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
   }
 }
 
-// Y[s, c] of every long slice s from its share partials p_0 .. p_{m-1}: lane
-// l adds p_l, p_{l+32}, ... in order (from zero), then the lanes meet in the
-// butterfly over strides 16, 8, 4, 2, 1.  One warp per (long slice, column);
-// the order depends on the share count alone.
+// Y[s, c] of every long slice s from its share partials p_0 .. p_{m-1}: 32
+// lane sums s_j = p_j + p_{j+32} + ... (in order, from zero), then the
+// butterfly s_j += s_{j^h}, h = 16, 8, 4, 2, 1.  One warp per long slice:
+// lane j loads whole partial rows (16 columns at a time, 16-byte vectors),
+// so every load of the warp is in flight at once.  The order depends on the
+// share count alone.
 template <typename T>
 __global__ void __launch_bounds__(256) share_combine_kernel(const T *__restrict__ P,
                                                             const int4 *__restrict__ longs,
                                                             int64_t n_long, int w,
                                                             T *__restrict__ Y, int64_t ldy) {
+  constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
+  constexpr int CB = 16;              // columns per pass
+  using V = typename VecT<T, VW>::type;
+  using Ops = VecOps<T, VW>;
   const int lane = threadIdx.x & 31;
-  const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (item >= n_long * w) return;
-  const int64_t l = item / w;
-  const int c = (int)(item - l * w);
+  const int64_t l = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (l >= n_long) return;
   const int4 d = longs[l];  // {slice, first share, shares, 0}
-  T sum = T(0);
-  for (int q = lane; q < d.z; q += 32) sum = sum + P[(int64_t)(d.y + q) * kMaxBlockWidth + c];
+  // columns [c0, c0 + CB) of a partial row lie inside its kMaxBlockWidth
+  // slots (entries past w hold no result and are never stored)
+  for (int c0 = 0; c0 < w; c0 += CB) {
+    T s[CB];
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) sum = sum + __shfl_xor_sync(kFullMask, sum, off);
-  if (lane == 0) Y[(int64_t)d.x * ldy + c] = sum;
+    for (int e = 0; e < CB; ++e) s[e] = T(0);
+    // rows lane, lane + 32, ...: kRows of them loaded before their adds
+    constexpr int kRows = 4;
+    for (int q0 = lane; q0 < d.z; q0 += 32 * kRows) {
+      V v[kRows][CB / VW];
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        const int q = q0 + 32 * r;
+        const V *row = reinterpret_cast<const V *>(P + (int64_t)(d.y + q) * kMaxBlockWidth + c0);
+#pragma unroll
+        for (int k = 0; k < CB / VW; ++k) v[r][k] = q < d.z ? __ldcg(row + k) : V{};
+      }
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        if (q0 + 32 * r >= d.z) break;
+#pragma unroll
+        for (int k = 0; k < CB / VW; ++k) {
+          T x[VW];
+          Ops::unpack(v[r][k], x);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) s[k * VW + e] = s[k * VW + e] + x[e];
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+      for (int e = 0; e < CB; ++e) s[e] = s[e] + __shfl_xor_sync(kFullMask, s[e], h);
+    T out = s[0];
+#pragma unroll
+    for (int e = 1; e < CB; ++e)
+      if (lane == e) out = s[e];
+    if (lane < CB && c0 + lane < w) Y[(int64_t)d.x * ldy + c0 + lane] = out;
+  }
 }
 
 // ------------------------------------------------------------------ dispatch
@@ -444,8 +490,7 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
       VS_LAUNCH_CHECK();
     }
     if (m.n_long > 0) {
-      const int64_t warps = m.n_long * wb;
-      share_combine_kernel<T><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
+      share_combine_kernel<T><<<(unsigned)((m.n_long + 7) / 8), 256, 0, s>>>(
           static_cast<const T *>(m.partials), m.longs, m.n_long, wb, yp, Y.ld);
       VS_LAUNCH_CHECK();
     }
