@@ -89,7 +89,10 @@ class Clocks:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def count(self, t0: float) -> int:
+        return sum(1 for t, _ in self.lines if t >= t0)
 
     def __exit__(self, *exc):
         if self.proc:
@@ -100,10 +103,12 @@ class Clocks:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0: float = 0.0, t1: float = float("inf")):
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if not t0 <= t <= t1:
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -119,6 +124,20 @@ class Clocks:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def aggregate(ms_local: float, step_bytes: int, ws: int, device):
+    """Whole-job figures of N replicas: the slowest rank's ms per step, and the
+    bytes all ranks processed per second (GB/s) at that pace."""
+    t_max = ms_local
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    return t_max, step_bytes * ws / (t_max * 1e-3) / 1e9
 
 
 def source_digest() -> str:
@@ -348,27 +367,28 @@ def gpu_arm(args):
     launches0 = vs.kernel_launches()
     per = {name: [] for name, *_ in PRODUCTS}
     with Clocks(local) as clk:
+        time.sleep(0.5)  # the sampler is running before the timed steps start
         wall0 = time.perf_counter()
         for _ in range(args.steps):
             for p in PRODUCTS:
                 per[p[0]].extend(timed(lambda p=p: run(*p), 1))
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
-    launches = vs.kernel_launches() - launches0
+        launches = vs.kernel_launches() - launches0
+        # a short timed region sees few samples: keep the same load running,
+        # untimed, until the sampler has seen at least 3 (at most 5 s more)
+        t_end = time.perf_counter()
+        while clk.count(wall0) < 3 and time.perf_counter() - t_end < 5.0:
+            for p in PRODUCTS:
+                timed(lambda p=p: run(*p), 1)
+        clk_window = (wall0, time.perf_counter())
     if ws > 1:
         dist.barrier()
     ms_prod = {k: statistics.median(v) for k, v in per.items()}
     ms_mean = {k: statistics.mean(v) for k, v in per.items()}
     ms_step = sum(ms_prod.values())
     step_bytes = sum(nbytes.values())
-    t_local = ms_step
-    if ws > 1:
-        t = torch.tensor([t_local], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
-    else:
-        t_max = t_local
-    value = step_bytes * ws / (t_max * 1e-3) / 1e9
+    t_max, value = aggregate(ms_step, step_bytes, ws, dev)
 
     # ---- variants of the misaligned products (reported, not in the step)
     variants = {}
@@ -445,6 +465,18 @@ def gpu_arm(args):
                     "frac_of_measured": round(nbytes[k] / ms_prod[k] / 1e6 / peak, 4),
                     "bytes": nbytes[k]} for k in ms_prod}
     traffic = recorded_traffic(dom)
+    # the second roof: every stored entry brings a row of w values of X through
+    # L1 or shared memory, at most 128 bytes per clock per SM (nominal width)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk_now = clk.summary(*clk_window)
+    mhz = clk_now.get("sm_mhz") or clk_now.get("sm_max_mhz") or 2070.0
+    onchip_bytes = coo.nnz * WIDTH * 4
+    onchip_peak = 128.0 * n_sm * mhz * 1e6 / 1e9  # GB/s
+    onchip_ach = onchip_bytes / (ms_prod[dom] * 1e-3) / 1e9
+    onchip = {"bound": "l1/shared gather", "kernel": dom, "achieved": round(onchip_ach, 1),
+              "peak": round(onchip_peak, 1), "peak_kind": "nominal: 128 B/clk/SM x SMs x sampled SM clock",
+              "unit": "GB/s", "frac": round(onchip_ach / onchip_peak, 4),
+              "bytes_per_launch": onchip_bytes}
 
     # ---- CPU baseline: the float64 oracle on host cores (rank 0, N=1 only)
     cpu = None
@@ -473,11 +505,13 @@ def gpu_arm(args):
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "per": "one launch of the product's gather kernel (median of the timed reps)"},
+        "roofline_onchip": onchip,
         "host_us_per_call": round(host_us, 2),
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
-        "clocks": clk.summary(),
+        "clocks": dict(clk.summary(*clk_window),
+                       window="the timed steps, extended by untimed steps to 3 samples"),
         "gpu_launches": launches,
         "products": products,
         "misaligned_variants": variants,
