@@ -238,6 +238,37 @@ vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_
  */
 vs_status vs_attach_transpose(vs_handle A, cudaStream_t stream);
 
+/*
+ * vs_transpose -- a new handle holding the exact transpose of A as a matrix of
+ * its own ("Regridder", "API": .T, the exact transpose): same layout and
+ * dtype, the other major axis, shape n_cols x n_rows seen from the caller as
+ * the transpose (its rows are A's columns).  For CSR, slice j of the result
+ * lists the entries of A's column j in A's storage order.  The new handle
+ * owns its arrays; A is unchanged.  Synchronises `stream` once.
+ *   out   receives the handle (NULL on error); release with vs_destroy
+ */
+vs_status vs_transpose(vs_handle A, cudaStream_t stream, vs_handle *out);
+
+/*
+ * vs_scale_entries -- the hook of the conservative transpose ("Regridder",
+ * "API": it scales each entry of the exact transpose by a factor of its own
+ * and shares the indices of .T).  Returns a new CSR handle with A's sparsity
+ * pattern whose stored value e is A's value e times factors[e], rounded once
+ * in A's dtype.  The index arrays and kernel metadata are shared with A (not
+ * copied) and stay valid until both handles are destroyed; the new handle
+ * owns its values and scratch.  The factors themselves (cell sizes) are the
+ * caller's.
+ *   factors  device array of nnz values of A's dtype, in A's storage order
+ *            (the order of vs_export's values); caller-owned, read before the
+ *            call's work on `stream` completes
+ *   out      receives the handle (NULL on error); release with vs_destroy
+ * Errors: VS_ERR_LAYOUT for a VCS handle (a per-entry factor would split its
+ * runs, so no index array could be shared); VS_ERR_INVALID for NULL factors
+ * with nnz > 0.
+ */
+vs_status vs_scale_entries(vs_handle A, const void *factors, cudaStream_t stream,
+                           vs_handle *out);
+
 /* vs_info -- shape, layout and matrix-only kernel parameters of A. */
 vs_status vs_info(vs_handle A, vs_info_t *info);
 

@@ -74,12 +74,14 @@ def load() -> ctypes.CDLL:
         lib.vs_spmm_host.argtypes = [H, ctypes.POINTER(Dense), ctypes.POINTER(Dense), i32, i32, vp]
         lib.vs_spmm_noalloc.argtypes = [H, ctypes.POINTER(Dense), ctypes.POINTER(Dense), i32, vp]
         lib.vs_attach_transpose.argtypes = [H, vp]
+        lib.vs_transpose.argtypes = [H, vp, ctypes.POINTER(H)]
+        lib.vs_scale_entries.argtypes = [H, vp, vp, ctypes.POINTER(H)]
         lib.vs_info.argtypes = [H, ctypes.POINTER(Info)]
         lib.vs_export.argtypes = [H, ctypes.POINTER(Arrays)]
         lib.vs_handle_bytes.argtypes = [H, ctypes.POINTER(i64), ctypes.POINTER(i64)]
         lib.vs_destroy.argtypes = [H]
         for f in ("vs_build_csr", "vs_build_vcs", "vs_spmm", "vs_spmm_host", "vs_spmm_noalloc",
-                  "vs_attach_transpose",
+                  "vs_attach_transpose", "vs_transpose", "vs_scale_entries",
                   "vs_info", "vs_export", "vs_handle_bytes", "vs_destroy"):
             getattr(lib, f).restype = i32
         lib.vs_status_string.argtypes = [i32]

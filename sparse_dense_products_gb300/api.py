@@ -101,6 +101,26 @@ class SparseMatrix:
         L.check(L.load().vs_attach_transpose(self.handle, ctypes.c_void_p(_stream_ptr(self.device))))
         return self
 
+    def transpose(self) -> "SparseMatrix":
+        """A new matrix holding the exact transpose (shape swapped, other major axis)."""
+        h = ctypes.c_void_p()
+        L.check(L.load().vs_transpose(self.handle, ctypes.c_void_p(_stream_ptr(self.device)),
+                                      ctypes.byref(h)))
+        return SparseMatrix(h.value, (self.shape[1], self.shape[0]), self.device)
+
+    def scale_entries(self, factors: torch.Tensor) -> "SparseMatrix":
+        """A new CSR matrix sharing this one's indices, values[e] * factors[e]
+        (factors in storage order, the order of arrays()["values"])."""
+        _require_cuda(factors)
+        if factors.dtype != self.dtype or factors.numel() != self.info()["nnz"] or \
+                not factors.is_contiguous():
+            raise ValueError("factors must be a contiguous tensor of nnz values of the matrix dtype")
+        h = ctypes.c_void_p()
+        L.check(L.load().vs_scale_entries(self.handle, ctypes.c_void_p(factors.data_ptr()),
+                                          ctypes.c_void_p(_stream_ptr(self.device)),
+                                          ctypes.byref(h)))
+        return SparseMatrix(h.value, self.shape, self.device)
+
     def destroy(self) -> None:
         if self._h:
             L.check(L.load().vs_destroy(self._h))

@@ -55,6 +55,8 @@ struct Temp {
   }
 };
 
+}  // namespace
+
 vs_status dev_alloc(void **p, size_t bytes) {
   if (bytes == 0) bytes = 16;
   cudaError_t e = cudaMalloc(p, bytes);
@@ -65,6 +67,8 @@ vs_status dev_alloc(void **p, size_t bytes) {
   }
   return VS_OK;
 }
+
+namespace {
 
 inline unsigned grid_for(int64_t n, int per_block) {
   return (unsigned)std::max<int64_t>(1, (n + per_block - 1) / per_block);

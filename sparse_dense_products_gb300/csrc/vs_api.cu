@@ -16,6 +16,7 @@
 #include <mutex>
 #include <new>
 #include <string>
+#include <utility>
 
 #include "vs_internal.h"
 
@@ -52,10 +53,40 @@ int64_t Matrix::meta_bytes() const {
          (int64_t)dsize() * kMaxBlockWidth * n_shares + (int64_t)sizeof(int32_t) * (tp_chunks + 1);
 }
 
+namespace {
+// The index arrays of a matrix, freed when the last matrix using them goes.
+struct IndexArrays {
+  void *p[6];
+  ~IndexArrays() {
+    for (void *q : p)
+      if (q) cudaFree(q);
+  }
+};
+}  // namespace
+
+vs_status share_index_arrays(Matrix &m) {
+  if (m.index_owner) return VS_OK;
+  IndexArrays *ia = new (std::nothrow)
+      IndexArrays{{(void *)m.ptr, (void *)m.idx, (void *)m.vptr, (void *)m.blocks, (void *)m.longs,
+                   (void *)m.tp_bounds}};
+  if (!ia) {
+    set_error("host allocation failed");
+    return VS_ERR_ALLOC;
+  }
+  m.index_owner = std::shared_ptr<void>(ia, [](void *q) { delete static_cast<IndexArrays *>(q); });
+  return VS_OK;
+}
+
 void free_matrix(Matrix &m) {
-  for (void *p : {(void *)m.ptr, (void *)m.idx, m.vals, (void *)m.vptr, (void *)m.blocks,
-                  (void *)m.longs, m.partials, (void *)m.tp_bounds, (void *)m.err})
-    if (p) cudaFree(p);
+  if (m.index_owner) {
+    m.index_owner.reset();  // the index arrays go with their last user
+    for (void *p : {m.vals, m.partials, (void *)m.err})
+      if (p) cudaFree(p);
+  } else {
+    for (void *p : {(void *)m.ptr, (void *)m.idx, m.vals, (void *)m.vptr, (void *)m.blocks,
+                    (void *)m.longs, m.partials, (void *)m.tp_bounds, (void *)m.err})
+      if (p) cudaFree(p);
+  }
   m.ptr = m.idx = m.vptr = m.tp_bounds = nullptr;
   m.vals = m.partials = nullptr;
   m.blocks = nullptr;
@@ -195,6 +226,17 @@ vs_status frame(const Matrix &m, const vs_dense &B, const vs_dense &out, vs_dire
 
 }  // namespace
 
+namespace vs_derive {
+// values[e] * factors[e], one rounding in T (vs_scale_entries)
+template <typename T>
+__global__ void scale_values_kernel(const T *__restrict__ v, const T *__restrict__ f, int64_t n,
+                                    T *__restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = v[i] * f[i];
+}
+}  // namespace vs_derive
+
 extern "C" {
 
 vs_status vs_build_csr(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
@@ -302,6 +344,92 @@ vs_status vs_attach_transpose(vs_handle A, cudaStream_t stream) {
     return st;
   }
   A->T = t;
+  return VS_OK;
+}
+
+vs_status vs_transpose(vs_handle A, cudaStream_t stream, vs_handle *out) {
+  if (!out) return invalid("out handle pointer is NULL");
+  *out = nullptr;
+  if (!valid_handle(A)) return invalid("NULL handle");
+  vs_handle h = new (std::nothrow) vs_handle_s();
+  if (!h) {
+    set_error("host allocation failed");
+    return VS_ERR_ALLOC;
+  }
+  h->device = A->device;
+  vs_status st = build_transpose(A->A, h->A, stream);
+  if (st == VS_OK) {
+    // build_transpose stores A along its other axis; read as the same major
+    // axis, those arrays are the transpose Aᵀ (n_cols x n_rows)
+    Matrix &m = h->A;
+    std::swap(m.n_rows, m.n_cols);
+    m.major = A->A.major;
+    st = prepare_matrix(m, stream);
+  }
+  if (st != VS_OK) {
+    std::string msg = last_error();
+    cudaStreamSynchronize(stream);
+    free_matrix(h->A);
+    delete h;
+    set_error(msg);
+    return st;
+  }
+  *out = h;
+  return VS_OK;
+}
+
+vs_status vs_scale_entries(vs_handle A, const void *factors, cudaStream_t stream, vs_handle *out) {
+  if (!out) return invalid("out handle pointer is NULL");
+  *out = nullptr;
+  if (!valid_handle(A)) return invalid("NULL handle");
+  const Matrix &a = A->A;
+  if (a.layout != VS_LAYOUT_CSR) {
+    set_error("vs_scale_entries needs a CSR handle: a per-entry factor would split VCS runs");
+    return VS_ERR_LAYOUT;
+  }
+  if (a.nnz > 0 && !factors) return invalid("NULL factors");
+  VS_TRY(share_index_arrays(A->A));
+  vs_handle h = new (std::nothrow) vs_handle_s();
+  if (!h) {
+    set_error("host allocation failed");
+    return VS_ERR_ALLOC;
+  }
+  h->device = A->device;
+  Matrix &m = h->A;
+  m = a;  // shape, kernel parameters and the shared index arrays
+  m.vals = nullptr;
+  m.partials = nullptr;
+  m.err = nullptr;
+  auto fail = [&](vs_status st) {
+    std::string msg = last_error();
+    cudaStreamSynchronize(stream);
+    free_matrix(m);
+    delete h;
+    set_error(msg);
+    return st;
+  };
+  vs_status st = dev_alloc(&m.vals, m.dsize() * (size_t)(m.nnz + 16));
+  if (st == VS_OK && m.n_shares > 0)
+    st = dev_alloc(&m.partials, m.dsize() * kMaxBlockWidth * (size_t)m.n_shares);
+  if (st == VS_OK) st = dev_alloc((void **)&m.err, sizeof(int));
+  if (st != VS_OK) return fail(st);
+  if (cudaMemsetAsync(m.err, 0, sizeof(int), stream) != cudaSuccess)
+    return fail(cuda_status(cudaGetLastError(), "cudaMemsetAsync"));
+  if (m.nnz > 0) {
+    const unsigned grid = (unsigned)std::min<int64_t>(4096, (m.nnz + 255) / 256);
+    if (m.dtype == VS_F64)
+      vs_derive::scale_values_kernel<double><<<grid, 256, 0, stream>>>(
+          static_cast<const double *>(a.vals), static_cast<const double *>(factors), m.nnz,
+          static_cast<double *>(m.vals));
+    else
+      vs_derive::scale_values_kernel<float><<<grid, 256, 0, stream>>>(
+          static_cast<const float *>(a.vals), static_cast<const float *>(factors), m.nnz,
+          static_cast<float *>(m.vals));
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(cuda_status(e, "scale_values_kernel"));
+  }
+  *out = h;
   return VS_OK;
 }
 

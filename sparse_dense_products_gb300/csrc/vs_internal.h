@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <memory>
 #include <string>
 
 #include "../../include/vs.h"
@@ -94,6 +95,11 @@ struct Matrix {
   int tp_chunks = 0;                // C
   int32_t *tp_bounds = nullptr;     // [C+1] block boundaries of the groups
 
+  // When set, the index arrays (ptr, idx, vptr, blocks, longs, tp_bounds) are
+  // shared with other matrices (vs_scale_entries) and freed with the last
+  // reference; vals, partials and err always belong to this matrix.
+  std::shared_ptr<void> index_owner;
+
   size_t dsize() const { return dtype == VS_F64 ? 8 : 4; }
   int64_t layout_bytes() const;
   int64_t meta_bytes() const;
@@ -108,6 +114,8 @@ struct Scratch {
 };
 
 void free_matrix(Matrix &m);
+vs_status dev_alloc(void **p, size_t bytes);
+vs_status share_index_arrays(Matrix &m);
 
 }  // namespace vs
 
