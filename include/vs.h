@@ -219,6 +219,41 @@ vs_status vs_spmm_noalloc(vs_handle A, const vs_dense *B, const vs_dense *out, v
                           cudaStream_t stream);
 
 /*
+ * Normalized views ("Add CUDA transfer and matmul kernels for the normalized
+ * views": a view applies a transform g to the stored values and carries
+ * O(n_rows + n_cols) statistics; the recipes themselves are not defined
+ * there, so this is the generic hook).  The view of A is
+ *     V = diag(row_scale) . g(A) . diag(col_scale)
+ * with g applied to every stored value (a VCS matrix maps each run's value
+ * once, so the layout stays compressed).
+ */
+typedef enum {
+    VS_MAP_IDENTITY = 0,  /* g(v) = v */
+    VS_MAP_LOG1P = 1,     /* g(v) = log(1 + v), in the value dtype */
+    VS_MAP_SQRT = 2       /* g(v) = sqrt(v), in the value dtype */
+} vs_value_map;
+
+typedef struct {
+    vs_value_map map;
+    const void *row_scale; /* device, n_rows values of the dense dtype, or NULL (ones) */
+    const void *col_scale; /* device, n_cols values of the dense dtype, or NULL (ones) */
+} vs_view;
+
+/*
+ * vs_spmm_view -- out = V@B (dir VS_A_B) or B@V (VS_B_A) for the view V of A
+ * defined by `view` (NULL: V = A, the same as vs_spmm).  Variants and layout
+ * rules as for vs_spmm.  The scale of the output axis is applied when the
+ * gather stores a row (one multiply per element); the scale of the
+ * contracted axis pre-scales a copy of the dense operand held by the handle;
+ * a mapped g(A) is evaluated into handle scratch once per call.  Scratch
+ * grows on first use with a larger operand (stream-ordered).  With the same
+ * view and operands the result repeats bit for bit, like vs_spmm.
+ * Errors: as vs_spmm; VS_ERR_INVALID for an unknown map.
+ */
+vs_status vs_spmm_view(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direction dir,
+                       vs_variant variant, const vs_view *view, cudaStream_t stream);
+
+/*
  * vs_spmm_host -- vs_spmm with B and out in HOST memory (pinned memory is
  * fastest).  Copies B to device staging owned by the handle, runs vs_spmm on
  * `stream`, copies the result back and synchronises `stream` before

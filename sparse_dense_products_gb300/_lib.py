@@ -44,6 +44,14 @@ class Info(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class View(ctypes.Structure):
+    _fields_ = [("map", ctypes.c_int), ("row_scale", ctypes.c_void_p),
+                ("col_scale", ctypes.c_void_p)]
+
+
+MAPS = {"identity": 0, "log1p": 1, "sqrt": 2}
+
+
 class Arrays(ctypes.Structure):
     _fields_ = [("ptr", ctypes.c_void_p), ("indices", ctypes.c_void_p), ("values", ctypes.c_void_p),
                 ("value_ptr", ctypes.c_void_p), ("n_major", ctypes.c_int64), ("nnz", ctypes.c_int64),
@@ -73,6 +81,8 @@ def load() -> ctypes.CDLL:
         lib.vs_spmm.argtypes = [H, ctypes.POINTER(Dense), ctypes.POINTER(Dense), i32, i32, vp]
         lib.vs_spmm_host.argtypes = [H, ctypes.POINTER(Dense), ctypes.POINTER(Dense), i32, i32, vp]
         lib.vs_spmm_noalloc.argtypes = [H, ctypes.POINTER(Dense), ctypes.POINTER(Dense), i32, vp]
+        lib.vs_spmm_view.argtypes = [H, ctypes.POINTER(Dense), ctypes.POINTER(Dense), i32, i32,
+                                     ctypes.POINTER(View), vp]
         lib.vs_attach_transpose.argtypes = [H, vp]
         lib.vs_transpose.argtypes = [H, vp, ctypes.POINTER(H)]
         lib.vs_scale_entries.argtypes = [H, vp, vp, ctypes.POINTER(H)]
@@ -81,6 +91,7 @@ def load() -> ctypes.CDLL:
         lib.vs_handle_bytes.argtypes = [H, ctypes.POINTER(i64), ctypes.POINTER(i64)]
         lib.vs_destroy.argtypes = [H]
         for f in ("vs_build_csr", "vs_build_vcs", "vs_spmm", "vs_spmm_host", "vs_spmm_noalloc",
+                  "vs_spmm_view",
                   "vs_attach_transpose", "vs_transpose", "vs_scale_entries",
                   "vs_info", "vs_export", "vs_handle_bytes", "vs_destroy"):
             getattr(lib, f).restype = i32

@@ -212,11 +212,17 @@ def empty_out(A: SparseMatrix, w: int, direction: str = "A@B", dtype=None, devic
 
 
 def spmm(A: SparseMatrix, B: torch.Tensor, direction: str = "A@B",
-         variant: str = "deterministic", out: torch.Tensor | None = None) -> torch.Tensor:
+         variant: str = "deterministic", out: torch.Tensor | None = None, *,
+         map: str | None = None, row_scale: torch.Tensor | None = None,
+         col_scale: torch.Tensor | None = None) -> torch.Tensor:
     """``vs_spmm``: out = A @ B or out = B @ A on the current CUDA stream.
 
     A@B: B is n_cols x w with stride(1) == 1; B@A: B is w x n_rows with
     stride(0) == 1 (e.g. ``Bt.t()`` for a contiguous n_rows x w ``Bt``).
+
+    With ``map`` ("identity", "log1p", "sqrt"), ``row_scale`` (n_rows) or
+    ``col_scale`` (n_cols) the product uses the normalized view
+    diag(row_scale) g(A) diag(col_scale) instead of A (``vs_spmm_view``).
     """
     _require_cuda(B)
     w = B.shape[1] if direction == "A@B" else B.shape[0]
@@ -224,8 +230,20 @@ def spmm(A: SparseMatrix, B: torch.Tensor, direction: str = "A@B",
         out = empty_out(A, w, direction, B.dtype, B.device)
     _require_cuda(out)
     bd, od = _dense(B), _dense(out)
-    L.check(L.load().vs_spmm(A.handle, ctypes.byref(bd), ctypes.byref(od), _DIRS[direction],
-                             _VARIANTS[variant], ctypes.c_void_p(_stream_ptr(B.device))))
+    stream = ctypes.c_void_p(_stream_ptr(B.device))
+    if map is None and row_scale is None and col_scale is None:
+        L.check(L.load().vs_spmm(A.handle, ctypes.byref(bd), ctypes.byref(od), _DIRS[direction],
+                                 _VARIANTS[variant], stream))
+        return out
+    view = L.View(L.MAPS[map or "identity"], None, None)
+    for name, t, n in (("row_scale", row_scale, A.shape[0]), ("col_scale", col_scale, A.shape[1])):
+        if t is not None:
+            _require_cuda(t)
+            if t.dtype != B.dtype or t.numel() != n or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous tensor of {n} values of B's dtype")
+            setattr(view, name, t.data_ptr())
+    L.check(L.load().vs_spmm_view(A.handle, ctypes.byref(bd), ctypes.byref(od), _DIRS[direction],
+                                  _VARIANTS[variant], ctypes.byref(view), stream))
     return out
 
 

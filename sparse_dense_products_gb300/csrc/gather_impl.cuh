@@ -59,6 +59,7 @@ struct GatherArgs {
   int w;           // columns in this launch (<= kMaxBlockWidth)
   int n_x;         // rows of X (shared-memory variant: rows copied into the slab)
   void *partials;  // [n_shares][kMaxBlockWidth] of T
+  const void *yscale;  // optional: Y[s, :] *= yscale[s] at the store
 };
 
 // Where the rows X[t, :] come from.  Each lane holds the address of its own
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
   const int sub = lane / (Q * G);
   const T *__restrict__ X = static_cast<const T *>(a.X);
   T *__restrict__ Y = static_cast<T *>(a.Y);
+  const T *__restrict__ ys = static_cast<const T *>(a.yscale);
   T *__restrict__ P = static_cast<T *>(a.partials);
   const int w = a.w;
   const int npass = (w + TW - 1) / TW;
@@ -279,8 +281,14 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
         for (int cp = 0; cp < npass * TW; cp += TW) {
           const int col = cp + ql * VEC;
           gather_range<T, VEC, Q, G, NP, VCS>(sv, source(cp), n0, n1, slot, acc);
-          if (mine && slot == 0 && col < w)
+          if (mine && slot == 0 && col < w) {
+            if (ys) {
+              const T f = ys[s];
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) acc[0][e] = acc[0][e] * f;
+            }
             *reinterpret_cast<V *>(Y + (int64_t)s * a.ldy + col) = Ops::pack(acc[0]);
+          }
         }
       } else {
         // ---- share u of a chunk of a long slice: its partial goes to the
@@ -310,7 +318,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) share_combine_kernel(const T *__restrict__ P,
                                                             const int4 *__restrict__ longs,
                                                             int64_t n_long, int w,
-                                                            T *__restrict__ Y, int64_t ldy) {
+                                                            T *__restrict__ Y, int64_t ldy,
+                                                            const T *__restrict__ ys) {
   constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
   constexpr int CB = 16;              // columns per pass
   using V = typename VecT<T, VW>::type;
@@ -356,6 +365,7 @@ __global__ void __launch_bounds__(256) share_combine_kernel(const T *__restrict_
 #pragma unroll
     for (int e = 1; e < CB; ++e)
       if (lane == e) out = s[e];
+    if (ys) out = out * ys[d.x];
     if (lane < CB && c0 + lane < w) Y[(int64_t)d.x * ldy + c0 + lane] = out;
   }
 }
@@ -481,6 +491,7 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     a.w = wb;
     a.n_x = (int)m.n_minor;
     a.partials = m.partials;
+    a.yscale = Y.scale;
     int per_sm = 0;
     VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, Shape::kThreads, smem));
@@ -491,7 +502,8 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     }
     if (m.n_long > 0) {
       share_combine_kernel<T><<<(unsigned)((m.n_long + 7) / 8), 256, 0, s>>>(
-          static_cast<const T *>(m.partials), m.longs, m.n_long, wb, yp, Y.ld);
+          static_cast<const T *>(m.partials), m.longs, m.n_long, wb, yp, Y.ld,
+          static_cast<const T *>(Y.scale));
       VS_LAUNCH_CHECK();
     }
     c0 += wb;

@@ -235,7 +235,66 @@ __global__ void scale_values_kernel(const T *__restrict__ v, const T *__restrict
        i += (int64_t)gridDim.x * blockDim.x)
     out[i] = v[i] * f[i];
 }
+
+// Normalized views: g(v) elementwise, and row scalings of dense operands.
+template <typename T>
+__device__ __forceinline__ T apply_map(T v, int map) {
+  if (map == VS_MAP_LOG1P) return log1p(v);
+  if (map == VS_MAP_SQRT) return sqrt(v);
+  return v;
+}
+
+template <typename T>
+__global__ void map_values_kernel(const T *__restrict__ v, int64_t n, int map, T *__restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = apply_map(v[i], map);
+}
+
+// out[r, c] = X[r, c] * s[r] (out row stride w); in == out allowed for the
+// post-scaling of a result (ldx then its own stride, out = X)
+template <typename T>
+__global__ void scale_rows_kernel(const T *X, int64_t rows, int64_t ldx, int64_t w,
+                                  const T *__restrict__ s, T *out, int64_t ldo) {
+  const int64_t n = rows * w;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / w, c = i - r * w;
+    out[r * ldo + c] = X[r * ldx + c] * s[r];
+  }
+}
 }  // namespace vs_derive
+
+namespace vs {
+// The product in the slice frame: the aligned gather, or a misaligned variant.
+// Y.scale (an output-row scaling) is fused by the gather; the scatter
+// variants apply it with a pass over Y afterwards.
+vs_status run_product(vs_handle_s &h, const Matrix &m, const Matrix *t, DenseView X, DenseView Y,
+                      int64_t w, bool aligned, vs_variant variant, cudaStream_t stream) {
+  if (aligned) return launch_gather(m, X, Y, w, stream);
+  if (variant == VS_TRANSPOSED || (variant == VS_DETERMINISTIC && t)) {
+    if (!t) return invalid("VS_TRANSPOSED needs vs_attach_transpose first");
+    return launch_gather(*t, X, Y, w, stream);
+  }
+  DenseView Yp = Y;
+  Yp.scale = nullptr;
+  VS_TRY(variant == VS_ATOMIC ? launch_scatter_atomic(m, X, Yp, w, stream)
+                              : launch_scatter_two_phase(h, m, X, Yp, w, stream));
+  if (Y.scale && Y.rows > 0) {
+    const unsigned grid = (unsigned)std::min<int64_t>(4096, (Y.rows * w + 255) / 256);
+    if (m.dtype == VS_F64)
+      vs_derive::scale_rows_kernel<double><<<grid, 256, 0, stream>>>(
+          static_cast<const double *>(Y.p), Y.rows, Y.ld, w, static_cast<const double *>(Y.scale),
+          static_cast<double *>(Y.p), Y.ld);
+    else
+      vs_derive::scale_rows_kernel<float><<<grid, 256, 0, stream>>>(
+          static_cast<const float *>(Y.p), Y.rows, Y.ld, w, static_cast<const float *>(Y.scale),
+          static_cast<float *>(Y.p), Y.ld);
+    VS_LAUNCH_CHECK();
+  }
+  return VS_OK;
+}
+}  // namespace vs
 
 extern "C" {
 
@@ -265,19 +324,73 @@ vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direct
   bool aligned = false;
   VS_TRY(frame(A->A, *B, *out, dir, X, Y, w, aligned));
   if (w == 0 || Y.rows == 0) return VS_OK;
-  if (aligned) return launch_gather(A->A, X, Y, w, stream);
-  switch (variant) {
-    case VS_ATOMIC:
-      return launch_scatter_atomic(A->A, X, Y, w, stream);
-    case VS_TRANSPOSED:
-      if (!A->T) return invalid("VS_TRANSPOSED needs vs_attach_transpose first");
-      return launch_gather(*A->T, X, Y, w, stream);
-    case VS_TWO_PHASE:
-      return launch_scatter_two_phase(*A, A->A, X, Y, w, stream);
-    default:  // VS_DETERMINISTIC
-      if (A->T) return launch_gather(*A->T, X, Y, w, stream);
-      return launch_scatter_two_phase(*A, A->A, X, Y, w, stream);
+  return run_product(*A, A->A, A->T, X, Y, w, aligned, variant, stream);
+}
+
+vs_status vs_spmm_view(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direction dir,
+                       vs_variant variant, const vs_view *view, cudaStream_t stream) {
+  if (!view) return vs_spmm(A, B, out, dir, variant, stream);
+  if (!valid_handle(A)) return invalid("NULL handle");
+  if (!B || !out) return invalid("NULL operand descriptor");
+  if (variant != VS_DETERMINISTIC && variant != VS_ATOMIC && variant != VS_TRANSPOSED &&
+      variant != VS_TWO_PHASE)
+    return invalid("unknown variant");
+  if (view->map != VS_MAP_IDENTITY && view->map != VS_MAP_LOG1P && view->map != VS_MAP_SQRT)
+    return invalid("unknown value map");
+  DenseView X, Y;
+  int64_t w = 0;
+  bool aligned = false;
+  VS_TRY(frame(A->A, *B, *out, dir, X, Y, w, aligned));
+  if (w == 0 || Y.rows == 0) return VS_OK;
+  if (variant == VS_TRANSPOSED && !A->T) return invalid("VS_TRANSPOSED needs vs_attach_transpose first");
+  // views of the stored matrices (nothing here is freed: the arrays stay the handle's)
+  Matrix m = A->A, tv;
+  const Matrix *t = nullptr;
+  if (A->T) {
+    tv = *A->T;
+    t = &tv;
   }
+  if (view->map != VS_MAP_IDENTITY) {
+    auto map_into = [&](Matrix &mm, Scratch &dst) -> vs_status {
+      const bool vcs = mm.layout == VS_LAYOUT_VCS;
+      const int64_t n = vcs ? mm.R : mm.nnz;
+      const size_t es = vcs ? sizeof(float) : mm.dsize();
+      VS_TRY(dst.reserve(es * (size_t)(n + 16), stream));
+      if (n > 0) {
+        const unsigned grid = (unsigned)std::min<int64_t>(4096, (n + 255) / 256);
+        if (!vcs && mm.dtype == VS_F64)
+          vs_derive::map_values_kernel<double><<<grid, 256, 0, stream>>>(
+              static_cast<const double *>(mm.vals), n, (int)view->map, static_cast<double *>(dst.p));
+        else
+          vs_derive::map_values_kernel<float><<<grid, 256, 0, stream>>>(
+              static_cast<const float *>(mm.vals), n, (int)view->map, static_cast<float *>(dst.p));
+        VS_LAUNCH_CHECK();
+      }
+      mm.vals = dst.p;
+      return VS_OK;
+    };
+    VS_TRY(map_into(m, A->view_vals));
+    if (t) VS_TRY(map_into(tv, A->view_tvals));
+  }
+  // the contracted axis scales X (a scaled copy); the output axis scales Y rows
+  const void *xs = dir == VS_A_B ? view->col_scale : view->row_scale;
+  Y.scale = dir == VS_A_B ? view->row_scale : view->col_scale;
+  if (xs && X.rows > 0) {
+    const size_t es = m.dtype == VS_F64 ? 8 : 4;
+    VS_TRY(A->view_X.reserve(es * (size_t)(X.rows * w + 16), stream));
+    const unsigned grid = (unsigned)std::min<int64_t>(4096, (X.rows * w + 255) / 256);
+    if (m.dtype == VS_F64)
+      vs_derive::scale_rows_kernel<double><<<grid, 256, 0, stream>>>(
+          static_cast<const double *>(X.p), X.rows, X.ld, w, static_cast<const double *>(xs),
+          static_cast<double *>(A->view_X.p), w);
+    else
+      vs_derive::scale_rows_kernel<float><<<grid, 256, 0, stream>>>(
+          static_cast<const float *>(X.p), X.rows, X.ld, w, static_cast<const float *>(xs),
+          static_cast<float *>(A->view_X.p), w);
+    VS_LAUNCH_CHECK();
+    X = DenseView{A->view_X.p, X.rows, w};
+  }
+  return run_product(*A, m, t, X, Y, w, aligned, variant, stream);
 }
 
 vs_status vs_spmm_noalloc(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direction dir,

@@ -126,6 +126,7 @@ struct vs_handle_s {
   vs::Scratch tp_partials;   // two-phase chunk partials
   vs::Scratch tp_table;      // two-phase tile offsets
   vs::Scratch stage_B, stage_out;  // host-operand staging (vs_spmm_host)
+  vs::Scratch view_vals, view_tvals, view_X;  // normalized views: mapped values, scaled X
 };
 
 namespace vs {
@@ -154,6 +155,9 @@ struct DenseView {
   void *p;
   int64_t rows;
   int64_t ld;
+  // Output only: when set, row r of the result is multiplied by scale[r]
+  // before it is stored (the gather fuses it; other kernels take a pass).
+  const void *scale = nullptr;
 };
 
 // Aligned gather: Y[s, 0:w] = sum over entries (t, a) of slice s of a * X[t, 0:w].
