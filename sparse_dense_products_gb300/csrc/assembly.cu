@@ -714,7 +714,8 @@ vs_status prepare_matrix(Matrix &m, cudaStream_t s) {
   if (n_long > 0) {
     VS_TRY(dev_alloc((void **)&m.longs, sizeof(int4) * n_long));
     VS_CUDA(cudaMemcpyAsync(m.longs, longs.data(), sizeof(int4) * n_long, cudaMemcpyHostToDevice, s));
-    VS_TRY(dev_alloc(&m.partials, m.dsize() * kMaxBlockWidth * n_shares));
+    // share partials hold sums of the operand type: float64 covers every product
+    VS_TRY(dev_alloc(&m.partials, sizeof(double) * kMaxBlockWidth * n_shares));
   }
   VS_TRY(dev_alloc((void **)&m.err, sizeof(int)));
   VS_CUDA(cudaMemsetAsync(m.err, 0, sizeof(int), s));

@@ -1,5 +1,5 @@
 // gather_f32_csr.cu -- instantiates the aligned gather (gather_impl.cuh) for
-// float values, CSR layout, with X read through L1; hands the product to the
+// float values, CSR layout, float operands, with X read through L1; hands the product to the
 // shared-memory-slab instantiation (gather_f32_csr_xs.cu) when X fits it.
 #include "gather_impl.cuh"
 
@@ -7,7 +7,7 @@ namespace vs {
 vs_status launch_gather_f32_csr_xs(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s);
 
 vs_status launch_gather_f32_csr(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s) {
-  if (gather_detail::slab_fits<float, false>(m, X, Y, w)) return launch_gather_f32_csr_xs(m, X, Y, w, s);
-  return gather_detail::launch_typed<float, false, false>(m, X, Y, w, s);
+  if (gather_detail::slab_fits<float, float, false>(m, X, Y, w)) return launch_gather_f32_csr_xs(m, X, Y, w, s);
+  return gather_detail::launch_typed<float, float, false, false>(m, X, Y, w, s);
 }
 }  // namespace vs

@@ -1,0 +1,9 @@
+// gather_f64_vcs_xs.cu -- instantiates the aligned gather (gather_impl.cuh) for
+// VCS (float run values), double operands and sums, with X held in a shared-memory slab.
+#include "gather_impl.cuh"
+
+namespace vs {
+vs_status launch_gather_f64_vcs_xs(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s) {
+  return gather_detail::launch_typed<double, float, true, true>(m, X, Y, w, s);
+}
+}  // namespace vs

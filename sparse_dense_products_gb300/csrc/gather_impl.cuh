@@ -89,8 +89,8 @@ struct XSource<T, VEC, true> {
 
 // Sums entries [n0, n1) of one slice for this lane's VEC columns and runs the
 // fixed tree; acc[0] holds the result in the slice's slot-0 lanes.
-template <typename T, int VEC, int Q, int G, int NP, bool VCS, class XSrc>
-__device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const XSrc &xs, int n0,
+template <typename T, typename TV, int VEC, int Q, int G, int NP, bool VCS, class XSrc>
+__device__ __forceinline__ void gather_range(const Staged<TV, VCS> &sv, const XSrc &xs, int n0,
                                              int n1, int slot, T (&acc)[NP][VEC]) {
   using V = typename VecT<T, VEC>::type;
   using Ops = VecOps<T, VEC>;
@@ -109,7 +109,7 @@ __device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const XSr
 #pragma unroll
     for (int i = 0; i < 2 * NP; ++i) {
       j[i] = sv.idx[n + i * G];
-      av[i] = sv.vals[n + i * G];
+      av[i] = static_cast<T>(sv.vals[n + i * G]);
     }
     V x[2 * NP];
 #pragma unroll
@@ -128,7 +128,7 @@ __device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const XSr
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
       j[i] = sv.idx[n + i * G];
-      av[i] = sv.vals[n + i * G];
+      av[i] = static_cast<T>(sv.vals[n + i * G]);
     }
     V x[NP];
 #pragma unroll
@@ -147,7 +147,7 @@ __device__ __forceinline__ void gather_range(const Staged<T, VCS> &sv, const XSr
     const int nn = n + i * G;
     if (nn < n1) {
       const int jj = sv.idx[nn];
-      const T a = sv.vals[nn];
+      const T a = static_cast<T>(sv.vals[nn]);
       const V x = xs.load(jj);
       T xe[VEC];
       Ops::unpack(x, xe);
@@ -193,7 +193,7 @@ struct GatherShape {
                 "each stage buffer must always go to the same expanding warp");
 };
 
-template <typename T, int VEC, int Q, int G, int NP, bool VCS, bool XS>
+template <typename T, typename TV, int VEC, int Q, int G, int NP, bool VCS, bool XS>
 __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS, VCS>::kMinCtas)
     gather_kernel(const GatherArgs a) {
   using V = typename VecT<T, VEC>::type;
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
   constexpr int S = 32 / (Q * G);  // slices per warp work unit
   constexpr int TW = Q * VEC;      // columns per pass
   extern __shared__ __align__(128) unsigned char smem[];
-  const Pipe<T, VCS, NS> pipe{smem};
+  const Pipe<TV, VCS, NS> pipe{smem};
   constexpr int GW = NW / Shape::kGroups;  // consumer warps per group
   pipe.init(GW);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
 
   // XS: copy X[:, 0:w) into the slab, pass by pass ([pass][row][TW], columns
   // past w zero), while the producer already streams the first blocks
-  T *slab = reinterpret_cast<T *>(smem + PipeLayout<T, VCS, NS>::kExtra);
+  T *slab = reinterpret_cast<T *>(smem + PipeLayout<TV, VCS, NS>::kExtra);
   if constexpr (XS) {
     const int nv = a.n_x * Q;  // vectors per pass
     for (int p = 0; p < npass; ++p)
@@ -260,8 +260,8 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
        b += Shape::kGroups * gridDim.x, i += Shape::kGroups) {
     if (!pipe.acquire(i, a.st)) return;
     unsigned char *buf = pipe.buf(i % NS);
-    const Block k = stage_desc<T, VCS>(buf);
-    const Staged<T, VCS> sv = stage_views<T, VCS>(k, buf);
+    const Block k = stage_desc<TV, VCS>(buf);
+    const Staged<TV, VCS> sv = stage_views<TV, VCS>(k, buf);
     const int units = block_units(k, S);
     T acc[NP][VEC];
     // work units go round-robin to the consumer warps, continuing across blocks
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
         }
         for (int cp = 0; cp < npass * TW; cp += TW) {
           const int col = cp + ql * VEC;
-          gather_range<T, VEC, Q, G, NP, VCS>(sv, source(cp), n0, n1, slot, acc);
+          gather_range<T, TV, VEC, Q, G, NP, VCS>(sv, source(cp), n0, n1, slot, acc);
           if (mine && slot == 0 && col < w) {
             if (ys) {
               const T f = ys[s];
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
         const int n0 = sub == 0 ? na : 0, n1 = sub == 0 ? nb : 0;
         for (int cp = 0; cp < npass * TW; cp += TW) {
           const int col = cp + ql * VEC;
-          gather_range<T, VEC, Q, G, NP, VCS>(sv, source(cp), n0, n1, slot, acc);
+          gather_range<T, TV, VEC, Q, G, NP, VCS>(sv, source(cp), n0, n1, slot, acc);
           if (sub == 0 && slot == 0 && col < w)
             *reinterpret_cast<V *>(P + (int64_t)(k.first + u) * kMaxBlockWidth + col) =
                 Ops::pack(acc[0]);
@@ -382,36 +382,36 @@ using KernelPtr = void (*)(const GatherArgs);
 #endif
 constexpr int kMaxSlots = VS_MAX_SLOTS;
 
-template <typename T, int VEC, int Q, int G, bool VCS, bool XS>
+template <typename T, typename TV, int VEC, int Q, int G, bool VCS, bool XS>
 KernelPtr<T, VCS> pick_np(int np) {
   if constexpr (G == kMaxSlots || G * Q == 32) {
     if constexpr (Q * G * 2 <= 64)
-      if (np == 2) return gather_kernel<T, VEC, Q, G, 2, VCS, XS>;
+      if (np == 2) return gather_kernel<T, TV, VEC, Q, G, 2, VCS, XS>;
     if constexpr (Q * G * 4 <= 128)
-      if (np == 4) return gather_kernel<T, VEC, Q, G, 4, VCS, XS>;
+      if (np == 4) return gather_kernel<T, TV, VEC, Q, G, 4, VCS, XS>;
   }
-  return np == 1 ? gather_kernel<T, VEC, Q, G, 1, VCS, XS> : nullptr;
+  return np == 1 ? gather_kernel<T, TV, VEC, Q, G, 1, VCS, XS> : nullptr;
 }
 
-template <typename T, int VEC, int Q, bool VCS, bool XS>
+template <typename T, typename TV, int VEC, int Q, bool VCS, bool XS>
 KernelPtr<T, VCS> pick_g(int G, int np) {
   switch (G) {
-    case 1: return pick_np<T, VEC, Q, 1, VCS, XS>(np);
-    case 2: return pick_np<T, VEC, Q, 2, VCS, XS>(np);
-    case 4: return pick_np<T, VEC, Q, 4, VCS, XS>(np);
-    case 8: return pick_np<T, VEC, Q, 8, VCS, XS>(np);
-    case 16: if constexpr (kMaxSlots >= 16 && Q <= 2) return pick_np<T, VEC, Q, 16, VCS, XS>(np); break;
-    case 32: if constexpr (kMaxSlots >= 32 && Q == 1) return pick_np<T, VEC, Q, 32, VCS, XS>(np); break;
+    case 1: return pick_np<T, TV, VEC, Q, 1, VCS, XS>(np);
+    case 2: return pick_np<T, TV, VEC, Q, 2, VCS, XS>(np);
+    case 4: return pick_np<T, TV, VEC, Q, 4, VCS, XS>(np);
+    case 8: return pick_np<T, TV, VEC, Q, 8, VCS, XS>(np);
+    case 16: if constexpr (kMaxSlots >= 16 && Q <= 2) return pick_np<T, TV, VEC, Q, 16, VCS, XS>(np); break;
+    case 32: if constexpr (kMaxSlots >= 32 && Q == 1) return pick_np<T, TV, VEC, Q, 32, VCS, XS>(np); break;
   }
   return nullptr;
 }
 
-template <typename T, int VEC, bool VCS, bool XS>
+template <typename T, typename TV, int VEC, bool VCS, bool XS>
 KernelPtr<T, VCS> pick_q(int Q, int G, int np) {
   switch (Q) {
-    case 1: return pick_g<T, VEC, 1, VCS, XS>(G, np);
-    case 2: return pick_g<T, VEC, 2, VCS, XS>(G, np);
-    case 4: return pick_g<T, VEC, 4, VCS, XS>(G, np);
+    case 1: return pick_g<T, TV, VEC, 1, VCS, XS>(G, np);
+    case 2: return pick_g<T, TV, VEC, 2, VCS, XS>(G, np);
+    case 4: return pick_g<T, TV, VEC, 4, VCS, XS>(G, np);
   }
   return nullptr;
 }
@@ -435,20 +435,22 @@ Tiling gather_tiling(int wb, const void *xp, const void *yp, int64_t ldx, int64_
 
 // Shared memory per CTA beyond the pipeline that the X slab may take.
 constexpr int64_t kSmemOptIn = 227 * 1024;
-template <typename T, bool VCS>
+template <typename TV, bool VCS>
 constexpr int64_t slab_budget() {
-  return kSmemOptIn - pipe_smem_bytes<T, VCS, GatherShape<true, VCS>::kStageBufs>(0);
+  return kSmemOptIn - pipe_smem_bytes<TV, VCS, GatherShape<true, VCS>::kStageBufs>(0);
 }
 
 // Whether X fits the shared-memory slab for at least one column pass.
-template <typename T, bool VCS>
+template <typename T, typename TV, bool VCS>
 bool slab_fits(const Matrix &m, DenseView X, DenseView Y, int64_t w) {
   const int wb = (int)std::min<int64_t>(kMaxBlockWidth, w);
   const Tiling t = gather_tiling<T>(wb, X.p, Y.p, X.ld, Y.ld);
-  return m.n_minor > 0 && m.n_minor * t.TW * (int64_t)sizeof(T) <= slab_budget<T, VCS>();
+  return m.n_minor > 0 && m.n_minor * t.TW * (int64_t)sizeof(T) <= slab_budget<TV, VCS>();
 }
 
-template <typename T, bool VCS, bool XS>
+// T: the dense operands and sums; TV: the stored values (float for VCS, and
+// for a float CSR matrix with double operands).
+template <typename T, typename TV, bool VCS, bool XS>
 vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s) {
   constexpr int VW = 16 / sizeof(T);
   using Shape = GatherShape<XS, VCS>;
@@ -464,7 +466,7 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     int64_t slab = 0;
     if constexpr (XS) {
       const int64_t pass = m.n_minor * t.TW * (int64_t)sizeof(T);
-      const int64_t fit = slab_budget<T, VCS>() / pass;  // column passes the slab holds
+      const int64_t fit = slab_budget<TV, VCS>() / pass;  // column passes the slab holds
       if (fit < 1) {
         set_error("dense operand does not fit the shared-memory slab");
         return VS_ERR_UNSUPPORTED;
@@ -474,13 +476,13 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     }
     const int G = std::min(std::min(m.g, kMaxSlots), 32 / t.Q);
     const int NP = m.g / G;
-    KernelPtr<T, VCS> k = t.vec ? pick_q<T, VW, VCS, XS>(t.Q, G, NP)
-                                : pick_q<T, 1, VCS, XS>(t.Q, G, NP);
+    KernelPtr<T, VCS> k = t.vec ? pick_q<T, TV, VW, VCS, XS>(t.Q, G, NP)
+                                : pick_q<T, TV, 1, VCS, XS>(t.Q, G, NP);
     if (!k) {
       set_error("no gather kernel for this width and group size");
       return VS_ERR_UNSUPPORTED;
     }
-    const int smem = pipe_smem_bytes<T, VCS, Shape::kStageBufs>((int)slab);
+    const int smem = pipe_smem_bytes<TV, VCS, Shape::kStageBufs>((int)slab);
     GatherArgs a;
     a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
                        nullptr, 0, 0, 0};

@@ -1,0 +1,9 @@
+// gather_mix_csr_xs.cu -- instantiates the aligned gather (gather_impl.cuh) for
+// float values, CSR layout, double operands and sums, with X held in a shared-memory slab.
+#include "gather_impl.cuh"
+
+namespace vs {
+vs_status launch_gather_mix_csr_xs(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s) {
+  return gather_detail::launch_typed<double, float, false, true>(m, X, Y, w, s);
+}
+}  // namespace vs

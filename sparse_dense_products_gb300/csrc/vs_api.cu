@@ -50,7 +50,7 @@ int64_t Matrix::layout_bytes() const {
 
 int64_t Matrix::meta_bytes() const {
   return (int64_t)sizeof(int4) * 3 * n_blocks + (int64_t)sizeof(int4) * n_long + (int64_t)sizeof(int) +
-         (int64_t)dsize() * kMaxBlockWidth * n_shares + (int64_t)sizeof(int32_t) * (tp_chunks + 1);
+         (int64_t)sizeof(double) * kMaxBlockWidth * n_shares + (int64_t)sizeof(int32_t) * (tp_chunks + 1);
 }
 
 namespace {
@@ -171,8 +171,11 @@ int64_t extent_bytes(const vs_dense &d) {
 vs_status frame(const Matrix &m, const vs_dense &B, const vs_dense &out, vs_direction dir,
                 DenseView &X, DenseView &Y, int64_t &w, bool &aligned) {
   if (dir != VS_A_B && dir != VS_B_A) return invalid("unknown direction");
-  if (B.dtype != m.dtype || out.dtype != m.dtype) {
-    set_error("B and out must have the matrix dtype (VCS: float32)");
+  // operands of the matrix dtype, or float64 operands with a float32 (or
+  // VCS) matrix: float values, float64 products and sums
+  const bool mixed = B.dtype == VS_F64 && m.dtype == VS_F32;
+  if (B.dtype != out.dtype || (B.dtype != m.dtype && !mixed)) {
+    set_error("B and out must have the matrix dtype, or float64 with a float32/VCS matrix");
     return VS_ERR_INVALID;
   }
   if (B.rows < 0 || B.cols < 0 || out.rows < 0 || out.cols < 0) return invalid("negative shape");
@@ -221,6 +224,7 @@ vs_status frame(const Matrix &m, const vs_dense &B, const vs_dense &out, vs_dire
     }
   }
   aligned = (dir == VS_A_B) == (m.major == VS_MAJOR_ROW);
+  X.f64 = Y.f64 = B.dtype == VS_F64;
   return VS_OK;
 }
 
@@ -276,13 +280,18 @@ vs_status run_product(vs_handle_s &h, const Matrix &m, const Matrix *t, DenseVie
     if (!t) return invalid("VS_TRANSPOSED needs vs_attach_transpose first");
     return launch_gather(*t, X, Y, w, stream);
   }
+  if (X.f64 && m.dtype == VS_F32) {
+    set_error("float64 operands with a float32/VCS matrix: misaligned products need the "
+              "transposed route (vs_attach_transpose)");
+    return VS_ERR_UNSUPPORTED;
+  }
   DenseView Yp = Y;
   Yp.scale = nullptr;
   VS_TRY(variant == VS_ATOMIC ? launch_scatter_atomic(m, X, Yp, w, stream)
                               : launch_scatter_two_phase(h, m, X, Yp, w, stream));
   if (Y.scale && Y.rows > 0) {
     const unsigned grid = (unsigned)std::min<int64_t>(4096, (Y.rows * w + 255) / 256);
-    if (m.dtype == VS_F64)
+    if (Y.f64)
       vs_derive::scale_rows_kernel<double><<<grid, 256, 0, stream>>>(
           static_cast<const double *>(Y.p), Y.rows, Y.ld, w, static_cast<const double *>(Y.scale),
           static_cast<double *>(Y.p), Y.ld);
@@ -376,10 +385,10 @@ vs_status vs_spmm_view(vs_handle A, const vs_dense *B, const vs_dense *out, vs_d
   const void *xs = dir == VS_A_B ? view->col_scale : view->row_scale;
   Y.scale = dir == VS_A_B ? view->row_scale : view->col_scale;
   if (xs && X.rows > 0) {
-    const size_t es = m.dtype == VS_F64 ? 8 : 4;
+    const size_t es = X.f64 ? 8 : 4;
     VS_TRY(A->view_X.reserve(es * (size_t)(X.rows * w + 16), stream));
     const unsigned grid = (unsigned)std::min<int64_t>(4096, (X.rows * w + 255) / 256);
-    if (m.dtype == VS_F64)
+    if (X.f64)
       vs_derive::scale_rows_kernel<double><<<grid, 256, 0, stream>>>(
           static_cast<const double *>(X.p), X.rows, X.ld, w, static_cast<const double *>(xs),
           static_cast<double *>(A->view_X.p), w);
@@ -388,7 +397,9 @@ vs_status vs_spmm_view(vs_handle A, const vs_dense *B, const vs_dense *out, vs_d
           static_cast<const float *>(X.p), X.rows, X.ld, w, static_cast<const float *>(xs),
           static_cast<float *>(A->view_X.p), w);
     VS_LAUNCH_CHECK();
+    const bool f64 = X.f64;
     X = DenseView{A->view_X.p, X.rows, w};
+    X.f64 = f64;
   }
   return run_product(*A, m, t, X, Y, w, aligned, variant, stream);
 }
@@ -404,6 +415,11 @@ vs_status vs_spmm_noalloc(vs_handle A, const vs_dense *B, const vs_dense *out, v
   if (w == 0 || Y.rows == 0) return VS_OK;
   if (aligned) return launch_gather(A->A, X, Y, w, stream);
   if (A->T) return launch_gather(*A->T, X, Y, w, stream);
+  if (X.f64 && A->A.dtype == VS_F32) {
+    set_error("float64 operands with a float32/VCS matrix: misaligned products need the "
+              "transposed route (vs_attach_transpose)");
+    return VS_ERR_UNSUPPORTED;
+  }
   return launch_scatter_two_phase_static(A->A, X, Y, w, stream);
 }
 
@@ -416,7 +432,7 @@ vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_
   bool aligned = false;
   VS_TRY(frame(A->A, *B_host, *out_host, dir, X, Y, w, aligned));
   if (w == 0 || Y.rows == 0) return VS_OK;
-  const size_t es = A->A.dsize();
+  const size_t es = X.f64 ? 8 : 4;
   const int64_t wpad = (w + 3) / 4 * 4;  // keep device rows 16-byte aligned
   VS_TRY(A->stage_B.reserve((size_t)std::max<int64_t>(X.rows, 1) * wpad * es, stream));
   VS_TRY(A->stage_out.reserve((size_t)Y.rows * wpad * es, stream));
@@ -523,7 +539,7 @@ vs_status vs_scale_entries(vs_handle A, const void *factors, cudaStream_t stream
   };
   vs_status st = dev_alloc(&m.vals, m.dsize() * (size_t)(m.nnz + 16));
   if (st == VS_OK && m.n_shares > 0)
-    st = dev_alloc(&m.partials, m.dsize() * kMaxBlockWidth * (size_t)m.n_shares);
+    st = dev_alloc(&m.partials, sizeof(double) * kMaxBlockWidth * (size_t)m.n_shares);
   if (st == VS_OK) st = dev_alloc((void **)&m.err, sizeof(int));
   if (st != VS_OK) return fail(st);
   if (cudaMemsetAsync(m.err, 0, sizeof(int), stream) != cudaSuccess)

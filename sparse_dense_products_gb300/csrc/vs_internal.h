@@ -85,7 +85,7 @@ struct Matrix {
   int64_t n_chunks = 0;         // chunks over all long slices
   int64_t n_shares = 0;         // shares over all long slices
   int4 *longs = nullptr;        // [n_long] {slice, first share, shares, 0}
-  void *partials = nullptr;     // [n_shares * kMaxBlockWidth] of dtype
+  void *partials = nullptr;     // [n_shares * kMaxBlockWidth] slots of 8 bytes (sums of the operand type)
   int *err = nullptr;           // device flag: a bounded wait gave up
   bool sorted_segments = false; // minor indices ascend inside every run / row
   int n_sm = 1;                 // multiprocessors of the device the matrix lives on
@@ -158,6 +158,9 @@ struct DenseView {
   // Output only: when set, row r of the result is multiplied by scale[r]
   // before it is stored (the gather fuses it; other kernels take a pass).
   const void *scale = nullptr;
+  // The dense operands are float64 (for a float32 or VCS matrix: the mixed
+  // products, float values with float64 operands and sums).
+  bool f64 = false;
 };
 
 // Aligned gather: Y[s, 0:w] = sum over entries (t, a) of slice s of a * X[t, 0:w].

@@ -217,8 +217,9 @@ def test_strided_operands_and_layout_errors():
     with pytest.raises(vs.VsError) as e:      # wrong shape
         vs.spmm(A, big[:100, :16], "A@B")
     assert e.value.status == 2
-    with pytest.raises(vs.VsError) as e:      # dtype mismatch
-        vs.spmm(A, big[:, :16].double(), "A@B")
+    with pytest.raises(vs.VsError) as e:      # dtype mismatch between B and out
+        vs.spmm(A, big[:, :16].double(), "A@B",
+                out=torch.empty((coo.n_rows, 16), device="cuda"))
     assert e.value.status == 1
     with pytest.raises(vs.VsError):           # transposed variant without a transpose
         vs.spmm(build(coo, "vcs", "col"), big[:, :16].contiguous(), "A@B", "transposed")
