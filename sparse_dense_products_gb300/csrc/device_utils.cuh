@@ -109,6 +109,33 @@ __device__ __forceinline__ double ld_shared<double>(uint32_t addr) {
   return v;
 }
 
+// Programmatic dependent launch: a kernel launched with launch_early may be
+// resident before the previous kernel of its stream has finished; this waits
+// until that kernel has completed and its memory is visible (a no-op when
+// there is no such dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launches `kernel` allowing it to start while the previous kernel of the
+// stream drains (the kernel must call grid_dependency_wait before it reads
+// or writes memory that kernel may touch).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_early(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Barrier over the first `threads` threads of the block (named barrier `id`).
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

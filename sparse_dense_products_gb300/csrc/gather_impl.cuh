@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
   const Pipe<TV, VCS, NS> pipe{smem};
   constexpr int GW = NW / Shape::kGroups;  // consumer warps per group
   pipe.init(GW);
+  grid_dependency_wait();  // may start while the previous kernel of the stream finishes
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (wid >= NW) {  // the producer warp(s)
     if constexpr (Shape::kExpanders == 0)
@@ -326,6 +327,7 @@ __global__ void __launch_bounds__(256) share_combine_kernel(const T *__restrict_
   using Ops = VecOps<T, VW>;
   const int lane = threadIdx.x & 31;
   const int64_t l = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  grid_dependency_wait();  // launched early: the gather's partials must be complete
   if (l >= n_long) return;
   const int4 d = longs[l];  // {slice, first share, shares, 0}
   // columns [c0, c0 + CB) of a partial row lie inside its kMaxBlockWidth
@@ -499,13 +501,14 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, Shape::kThreads, smem));
     const int64_t grid = std::min<int64_t>(m.n_blocks, (int64_t)std::max(1, per_sm) * m.n_sm);
     if (grid > 0) {
-      k<<<(unsigned)grid, Shape::kThreads, smem, s>>>(a);
+      VS_CUDA(launch_early(k, dim3((unsigned)grid), dim3(Shape::kThreads), smem, s, a));
       VS_LAUNCH_CHECK();
     }
     if (m.n_long > 0) {
-      share_combine_kernel<T><<<(unsigned)((m.n_long + 7) / 8), 256, 0, s>>>(
-          static_cast<const T *>(m.partials), m.longs, m.n_long, wb, yp, Y.ld,
-          static_cast<const T *>(Y.scale));
+      VS_CUDA(launch_early(share_combine_kernel<T>, dim3((unsigned)((m.n_long + 7) / 8)), dim3(256),
+                           0, s, static_cast<const T *>(m.partials),
+                           static_cast<const int4 *>(m.longs), m.n_long, wb, yp, Y.ld,
+                           static_cast<const T *>(Y.scale)));
       VS_LAUNCH_CHECK();
     }
     c0 += wb;
