@@ -28,6 +28,7 @@ constexpr int kStages = 4;
 constexpr int kConsumerThreads = kWarpsPerCta * 32;
 constexpr int kPipeThreads = kConsumerThreads + 32;  // plus the producer warp
 constexpr uint64_t kWaitLimitNs = 1000000000ull;     // 1 s
+constexpr int kFillRuns = 16;  // VCS expansion: blocks with at most this many runs fill run by run
 
 // Element capacity of each staged array, with room for 16-byte alignment slack.
 constexpr int kCapEntries = kBlockEntries + 8;
@@ -323,7 +324,8 @@ struct Pipe {
 
   // VCS, producer warp: block j (number b) has landed; write the run value of
   // each of its entries into the per-entry value array and mark the stage
-  // ready.  Run starts go into a bitmap over the block's entries; the run of
+  // ready.  A block of at most kFillRuns runs is filled run by run.
+  // Otherwise run starts go into a bitmap over the block's entries; the run of
   // entry n is then r0 - 1 + (run starts in [e0, n]).  A warp scan of the
   // words' popcounts gives each word the runs started before it; the words
   // are then independent, so the final pass has no chain between words.
@@ -339,6 +341,17 @@ struct Pipe {
     float *ev = reinterpret_cast<float *>(bp + LY::kEvals) - eb;
     uint32_t *bm = reinterpret_cast<uint32_t *>(bp + LY::kBitmap);
     int *wb = reinterpret_cast<int *>(bp + LY::kBases);
+    if (k.r1 - k.r0 <= kFillRuns) {
+      // few (long) runs: fill each run's entries with its value directly
+      for (int r = k.r0; r < k.r1; ++r) {
+        const int lo = max(vp[r], k.e0), hi = min(vp[r + 1], k.e1);
+        const float v = rv[r];
+        for (int n = lo + lane; n < hi; n += 32) ev[n] = v;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ready(s));
+      return;
+    }
     const int nwords = (k.e1 - eb + 31) / 32;
     for (int q = lane; q < nwords; q += 32) bm[q] = 0u;
     __syncwarp();
