@@ -62,11 +62,10 @@ struct StageLayout {
   static constexpr int kEvals = kRvals + (VCS ? kCapRuns * 4 : 0);                  // VCS only
   static constexpr int kBitmap = kEvals + (VCS ? kCapEntries * 4 : 0);              // VCS only
   static constexpr int kWords = (kCapEntries + 31) / 32;                           // bitmap words
-  static constexpr int kBases = kBitmap + (VCS ? (kWords * 4 + 15) / 16 * 16 : 0);  // VCS only
-  static constexpr int kDesc = kBases + (VCS ? (kWords * 4 + 15) / 16 * 16 : 0);
+  static constexpr int kDesc = kBitmap + (VCS ? (kWords * 4 + 15) / 16 * 16 : 0);
   static constexpr int kBytes = kDesc + 3 * 16;  // the block's descriptor, copied by the producer
   static_assert(kVals % 16 == 0 && kPtr % 16 == 0 && kVptr % 16 == 0 && kRvals % 16 == 0 &&
-                    kEvals % 16 == 0 && kBitmap % 16 == 0 && kBases % 16 == 0 && kDesc % 16 == 0 &&
+                    kEvals % 16 == 0 && kBitmap % 16 == 0 && kDesc % 16 == 0 &&
                     kBytes % 16 == 0,
                 "stage arrays must start on 16-byte boundaries");
 };
@@ -340,7 +339,6 @@ struct Pipe {
     const float *rv = reinterpret_cast<const float *>(bp + LY::kRvals) - align_down<4>(k.r0);
     float *ev = reinterpret_cast<float *>(bp + LY::kEvals) - eb;
     uint32_t *bm = reinterpret_cast<uint32_t *>(bp + LY::kBitmap);
-    int *wb = reinterpret_cast<int *>(bp + LY::kBases);
     if (k.r1 - k.r0 <= kFillRuns) {
       // few (long) runs: fill each run's entries with its value directly
       for (int r = k.r0; r < k.r1; ++r) {
@@ -360,25 +358,30 @@ struct Pipe {
       atomicOr(&bm[st >> 5], 1u << (st & 31));
     }
     __syncwarp();
+    // 32 words at a time: lane l holds word q0 + l and the runs started
+    // before it (a scan of the popcounts); the words then go round by shuffles
+    const unsigned le = lanemask_lt() | (1u << lane);
     int base = k.r0 - 1;  // runs started before word q0
     for (int q0 = 0; q0 < nwords; q0 += 32) {
       const bool has = q0 + lane < nwords;
-      const int c = has ? __popc(bm[q0 + lane]) : 0;
+      const uint32_t mine = has ? bm[q0 + lane] : 0u;
+      const int c = __popc(mine);
       int incl = c;  // inclusive scan of the popcounts over the lanes
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
         const int y = __shfl_up_sync(kFullMask, incl, d);
         if (lane >= d) incl += y;
       }
-      if (has) wb[q0 + lane] = base + incl - c;
-      base += __shfl_sync(kFullMask, incl, 31);
-    }
-    __syncwarp();
-    const unsigned le = lanemask_lt() | (1u << lane);
+      const int mybase = base + incl - c;
+      const int nq = min(32, nwords - q0);
 #pragma unroll 8
-    for (int q = 0; q < nwords; ++q) {
-      const int n = eb + 32 * q + lane;
-      if (n >= k.e0 && n < k.e1) ev[n] = rv[wb[q] + __popc(bm[q] & le)];
+      for (int q = 0; q < nq; ++q) {
+        const uint32_t word = __shfl_sync(kFullMask, mine, q);
+        const int wbase = __shfl_sync(kFullMask, mybase, q);
+        const int n = eb + 32 * (q0 + q) + lane;
+        if (n >= k.e0 && n < k.e1) ev[n] = rv[wbase + __popc(word & le)];
+      }
+      base += __shfl_sync(kFullMask, incl, 31);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(ready(s));
