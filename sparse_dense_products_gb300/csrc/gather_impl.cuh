@@ -43,10 +43,6 @@
 
 #include "stage.cuh"
 
-#ifndef VS_GATHER_MIN_CTAS
-#define VS_GATHER_MIN_CTAS 3
-#endif
-
 namespace vs {
 namespace gather_detail {
 
@@ -171,23 +167,23 @@ __device__ __forceinline__ void gather_range(const Staged<TV, VCS> &sv, const XS
 
 // Launch shape.  XS = true keeps X in shared memory: 16 consumer warps, 8
 // stage buffers, one CTA per SM, the slab taking the rest of the SM's shared
-// memory.  XS = false gathers X through L1: CSR runs 3 CTAs per SM of 8
-// consumer warps and 4 stage buffers, each with one producer warp; VCS runs
+// memory.  XS = false gathers X through L1: CSR runs 2 CTAs per SM of 12
+// consumer warps and 6 stage buffers, each with one producer warp; VCS runs
 // one CTA per SM of 20 consumer warps and 8 stage buffers.  Expanding VCS run
 // values is a chain of shared-memory round trips that one warp per SM cannot
 // keep ahead of the consumers, so VCS splits the producer into one issuing
 // warp and kExpanders expanding warps.
 template <bool XS, bool VCS>
 struct GatherShape {
-  static constexpr int kWarps = XS ? 16 : (VCS ? 20 : kWarpsPerCta);
-  static constexpr int kStageBufs = XS || VCS ? 8 : kStages;
+  static constexpr int kWarps = XS ? 16 : (VCS ? 20 : 12);
+  static constexpr int kStageBufs = XS || VCS ? 8 : 6;
   static constexpr int kExpanders = VCS ? 4 : 0;
   static constexpr int kThreads = (kWarps + 1 + kExpanders) * 32;
-  static constexpr int kMinCtas = XS || VCS ? 1 : VS_GATHER_MIN_CTAS;
+  static constexpr int kMinCtas = XS || VCS ? 1 : 2;
   // Consumer groups: block i of a CTA goes to group i mod kGroups only, so a
   // warp pays the per-block bookkeeping for 1 / kGroups of the blocks.  Each
   // stage buffer always serves the same group (kGroups divides the stages).
-  static constexpr int kGroups = XS || VCS ? 2 : 1;
+  static constexpr int kGroups = 2;
   static_assert(kStageBufs % kGroups == 0 && kWarps % kGroups == 0, "uneven consumer groups");
   static_assert(kExpanders == 0 || kStageBufs % kExpanders == 0,
                 "each stage buffer must always go to the same expanding warp");
