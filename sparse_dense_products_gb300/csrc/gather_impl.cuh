@@ -493,8 +493,7 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     a.partials = m.partials;
     a.yscale = Y.scale;
     int per_sm = 0;
-    VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, Shape::kThreads, smem));
+    VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(k), Shape::kThreads, smem, &per_sm));
     const int64_t grid = std::min<int64_t>(m.n_blocks, (int64_t)std::max(1, per_sm) * m.n_sm);
     if (grid > 0) {
       VS_CUDA(launch_early(k, dim3((unsigned)grid), dim3(Shape::kThreads), smem, s, a));

@@ -617,8 +617,7 @@ vs_status atomic_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     a.G = std::max(1, std::min(m.g, 32 / sh.Q));
     a.S = 32 / (sh.Q * a.G);
     int per_sm = 0;
-    VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kPipeThreads, smem));
+    VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(k), kPipeThreads, smem, &per_sm));
     const int64_t grid = std::min<int64_t>(m.n_blocks, (int64_t)std::max(1, per_sm) * m.n_sm);
     if (grid > 0) {
       k<<<(unsigned)grid, kPipeThreads, smem, s>>>(a);
@@ -651,7 +650,8 @@ vs_status two_phase_typed(vs_handle_s &h, const Matrix &m, DenseView X, DenseVie
         1, std::min<int64_t>(n_t, (kTwoPhaseSmem - stage) / row_bytes));
     const int64_t tiles = (n_t + tile_rows - 1) / tile_rows;
     const size_t smem = stage + (size_t)tile_rows * row_bytes;
-    VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTwoPhaseSmem));
+    int resident = 0;  // (raises the kernel's shared-memory limit once)
+    VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(k), kPipeThreads, (int)smem, &resident));
     TwoPhaseArgs a;
     a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
                        xp, X.ld, (int)sizeof(T), wb};
@@ -759,7 +759,8 @@ vs_status two_phase_static_typed(const Matrix &m, DenseView X, DenseView Y, int6
         1, std::min<int64_t>(n_t, (kTwoPhaseSmem - stage) / row_bytes));
     const int64_t tiles = (n_t + tile_rows - 1) / tile_rows;
     const size_t smem = stage + (size_t)tile_rows * row_bytes;
-    VS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTwoPhaseSmem));
+    int resident = 0;  // (raises the kernel's shared-memory limit once)
+    VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(k), kPipeThreads, (int)smem, &resident));
     TwoPhaseArgs a;
     a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
                        xp, X.ld, (int)sizeof(T), wb};

@@ -13,7 +13,10 @@
 // kernels": the same two binary choices as the host kernels.)
 #include <atomic>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <set>
+#include <tuple>
 #include <new>
 #include <string>
 #include <utility>
@@ -92,6 +95,31 @@ void free_matrix(Matrix &m) {
   m.blocks = nullptr;
   m.longs = nullptr;
   m.err = nullptr;
+}
+
+vs_status kernel_occupancy(const void *kernel, int threads, int smem, int *per_sm) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void *, int, int>, int> cache;
+  static std::set<std::pair<int, const void *>> raised;
+  int dev = 0;
+  VS_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_tuple(dev, kernel, threads, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *per_sm = it->second;
+    return VS_OK;
+  }
+  if (raised.insert({dev, kernel}).second) {
+    int optin = 0;
+    VS_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+    VS_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin));
+  }
+  int n = 0;
+  VS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, (size_t)smem));
+  cache.emplace(key, n);
+  *per_sm = n;
+  return VS_OK;
 }
 
 vs_status Scratch::reserve(size_t need, cudaStream_t s) {

@@ -179,6 +179,12 @@ vs_status launch_scatter_two_phase(vs_handle_s &h, const Matrix &m, DenseView X,
 vs_status launch_scatter_two_phase_static(const Matrix &m, DenseView X, DenseView Y, int64_t w,
                                           cudaStream_t s);
 
+// Resident CTAs per SM of `kernel` launched with `threads` threads and
+// `smem` bytes of dynamic shared memory, with the kernel allowed the SM's
+// whole opt-in shared memory.  Cached per (device, kernel, threads, smem), so
+// a product's host path makes no such query after its first call.
+vs_status kernel_occupancy(const void *kernel, int threads, int smem, int *per_sm);
+
 // Y[0:rows, 0:w] = 0 with row stride ld.
 vs_status launch_zero_fill(DenseView Y, int64_t w, size_t dsize, cudaStream_t s);
 
