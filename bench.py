@@ -422,6 +422,25 @@ def gpu_arm(args):
     except Exception as exc:  # reported, never fatal: it is a comparison, not the path
         cusparse = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
 
+    # ---- the same products with L2 warm (no flush between reps): labelled
+    # context, not the metric; near-equal times say the kernels are bound on
+    # chip, not by HBM
+    l2_warm = {}
+    for p in PRODUCTS:
+        for _ in range(3):
+            run(*p)
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(max(5, args.steps)):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run(*p)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        l2_warm[p[0]] = round(statistics.median(a.elapsed_time(b) for a, b in evs), 5)
+
     # ---- host cost of one asynchronous vs_spmm call (enqueue only)
     torch.cuda.synchronize()
     n_calls = 200
@@ -515,6 +534,7 @@ def gpu_arm(args):
         "gpu_launches": launches,
         "products": products,
         "misaligned_variants": variants,
+        "products_l2_warm_ms": l2_warm,
         "cusparse": cusparse,
         "assembly_ms": assembly,
         "wall_s_timed_region": round(wall, 3),
