@@ -1,5 +1,6 @@
 // device_utils.cuh -- small device helpers shared by the libvs kernels:
-// vector types, cache-hinted loads, vector reductions and a block scan.
+// vector types, shared and gather loads, vector reductions, scans, mbarrier
+// and bulk-copy wrappers, and the programmatic-dependent-launch helpers.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -49,23 +50,6 @@ struct VecOps {
     return v;
   }
 };
-
-// Read-only, read-once streams (indices, values): no L1 allocation.
-__device__ __forceinline__ int ld_stream(const int *p) {
-  int v;
-  asm("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ float ld_stream(const float *p) {
-  float v;
-  asm("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ double ld_stream(const double *p) {
-  double v;
-  asm("ld.global.nc.L1::no_allocate.f64 %0, [%1];" : "=d"(v) : "l"(p));
-  return v;
-}
 
 // Gathered dense rows: read-only, cached in L1.
 template <typename V>
@@ -260,20 +244,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// try_wait that may suspend the thread for up to `hint_ns` until the phase completes.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
-                                                    uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }

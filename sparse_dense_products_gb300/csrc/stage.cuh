@@ -253,30 +253,6 @@ __device__ __forceinline__ Staged<T, VCS> stage_views(const Block &k, unsigned c
   return v;
 }
 
-// VCS, one consumer warp: writes the run value of each entry n in [n0, n1)
-// into the stage buffer's per-entry value array (entries of different slices
-// or shares never overlap, so warps never write the same word).  Runs
-// [rlo, rhi) cover [n0, n1); one lane per entry, binary search over the runs.
-template <typename T, bool VCS>
-__device__ __forceinline__ void expand_runs(const Block &k, unsigned char *buf, int n0, int n1,
-                                            int rlo, int rhi) {
-  if (!VCS) return;
-  using LY = StageLayout<T, VCS>;
-  const int32_t *vp = reinterpret_cast<const int32_t *>(buf + LY::kVptr) - align_down<4>(k.r0);
-  const float *rv = reinterpret_cast<const float *>(buf + LY::kRvals) - align_down<4>(k.r0);
-  float *ev = reinterpret_cast<float *>(buf + LY::kEvals) - align_down<4>(k.e0);
-  for (int n = n0 + (int)(threadIdx.x & 31); n < n1; n += 32) {
-    int lo = rlo, hi = rhi - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (vp[mid] <= n) lo = mid;
-      else hi = mid - 1;
-    }
-    ev[n] = rv[lo];
-  }
-  __syncwarp();
-}
-
 // The pipeline's shared-memory control words.
 template <typename T, bool VCS, int NS = kStages>
 struct Pipe {
