@@ -464,7 +464,11 @@ vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_
   const int64_t wpad = (w + 3) / 4 * 4;  // keep device rows 16-byte aligned
   VS_TRY(A->stage_B.reserve((size_t)std::max<int64_t>(X.rows, 1) * wpad * es, stream));
   VS_TRY(A->stage_out.reserve((size_t)Y.rows * wpad * es, stream));
-  if (X.rows > 0)
+  // one linear copy when the host rows are already at the device pitch
+  if (X.rows > 0 && X.ld == wpad && w == wpad)
+    VS_CUDA(cudaMemcpyAsync(A->stage_B.p, X.p, (size_t)X.rows * wpad * es,
+                            cudaMemcpyHostToDevice, stream));
+  else if (X.rows > 0)
     VS_CUDA(cudaMemcpy2DAsync(A->stage_B.p, wpad * es, X.p, X.ld * es, w * es, X.rows,
                               cudaMemcpyHostToDevice, stream));
   vs_dense Bd{}, Od{};
@@ -476,8 +480,12 @@ vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_
     Od = vs_dense{A->stage_out.p, out_host->rows, out_host->cols, 1, wpad, out_host->dtype};
   }
   VS_TRY(vs_spmm(A, &Bd, &Od, dir, variant, stream));
-  VS_CUDA(cudaMemcpy2DAsync(Y.p, Y.ld * es, A->stage_out.p, wpad * es, w * es, Y.rows,
+  if (Y.ld == wpad && w == wpad)
+    VS_CUDA(cudaMemcpyAsync(Y.p, A->stage_out.p, (size_t)Y.rows * wpad * es,
                             cudaMemcpyDeviceToHost, stream));
+  else
+    VS_CUDA(cudaMemcpy2DAsync(Y.p, Y.ld * es, A->stage_out.p, wpad * es, w * es, Y.rows,
+                              cudaMemcpyDeviceToHost, stream));
   VS_CUDA(cudaStreamSynchronize(stream));
   return VS_OK;
 }

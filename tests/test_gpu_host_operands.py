@@ -1,0 +1,62 @@
+"""vs_spmm_host: the product with B and out in host memory (the end-to-end
+path of the benchmark) equals the device product bit for bit, for pinned and
+pageable buffers, pitched and strided host views, and leaves host memory
+outside the logical output untouched."""
+import pytest
+import torch
+
+import sparse_dense_products_gb300 as vs
+from sparse_dense_products_gb300 import build as vs_build
+from sparse_dense_products_gb300 import workloads as W
+
+from gpu_helpers import PRODUCTS, build, dense_operand
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device; none is visible"
+    vs_build.build()
+
+
+def _host_out(A, w, direction, dtype, pin, pad):
+    """A host output of the product's shape inside a wider (or taller) NaN-filled buffer."""
+    n_rows, n_cols = A.shape
+    if direction == "A@B":
+        big = torch.full((n_rows, w + pad), float("nan"), dtype=dtype)
+        return big, big[:, :w]
+    big = torch.full((w + pad, n_cols), float("nan"), dtype=dtype).t().contiguous().t()
+    return big, big[:w, :]
+
+
+@pytest.mark.parametrize("layout,major,direction", PRODUCTS)
+@pytest.mark.parametrize("w,pad,pin", [(16, 0, True), (5, 0, False), (8, 3, True)])
+def test_host_operands_match_device_product(layout, major, direction, w, pad, pin):
+    coo = W.random_coo(900, 700, 40_000, seed=61, values="counts", sort=False)
+    A = build(coo, layout, major)
+    A.attach_transpose()
+    B, _ = dense_operand(coo, direction, w, torch.float32, seed=3)
+    want = vs.spmm(A, B, direction).cpu()
+    Bh = B.cpu()
+    if pin:
+        Bh = Bh.pin_memory()
+    if direction == "B@A":           # the host operand keeps the width-contiguous layout
+        Bh = Bh.t().contiguous().t()
+    big, out = _host_out(A, w, direction, torch.float32, pin, pad)
+    vs.spmm_host(A, Bh, direction, "deterministic", out=out)
+    assert torch.equal(out, want)
+    if pad:
+        rest = big[:, w:] if direction == "A@B" else big[w:, :]
+        assert torch.isnan(rest).all(), "host memory outside the output was written"
+    A.destroy()
+
+
+def test_host_operands_mixed_precision():
+    coo = W.random_coo(500, 400, 20_000, seed=62, values="counts", sort=False)
+    A = build(coo, "vcs", "row")
+    B, _ = dense_operand(coo, "A@B", 16, torch.float64, seed=4)
+    want = vs.spmm(A, B, "A@B").cpu()
+    got = vs.spmm_host(A, B.cpu().pin_memory(), "A@B", "deterministic")
+    assert got.dtype == torch.float64 and torch.equal(got, want)
+    A.destroy()
