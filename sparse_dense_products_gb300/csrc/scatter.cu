@@ -15,8 +15,10 @@
 //    (balanced by entries, C fixed by the matrix) and Y into tiles of rows that
 //    fit in shared memory.  Phase 1: CTA (tile, group) streams its group's
 //    blocks in order and accumulates, in slice order and entry order, the
-//    contributions that land in its tile; each warp owns a band of the tile's
-//    rows, so no two threads update one element concurrently, and duplicate
+//    contributions that land in its tile; each warp owns the tile rows t with
+//    t mod 8 equal to its number (interleaved, so the popular rows of a skewed
+//    matrix spread over the warps), so no two threads update one element
+//    concurrently, and duplicate
 //    rows met together are applied one after another in entry order.  Phase 2
 //    adds the C group partials of every element in group order.  The order of
 //    every element's sum therefore depends on the matrix alone.
@@ -191,12 +193,20 @@ struct PrepLayout {
 
 constexpr int kQueueCap = 64;  // per-warp queue of in-band records
 
+// Two-phase CTA: kWarpsPerCta consumer warps, one warp issuing the copies and
+// kPreparers warps turning landed blocks into records (block i goes to
+// preparer i mod kPreparers; it divides kStages, so a stage always goes to
+// the same preparer and a parity wait never sees an old phase).
+constexpr int kPreparers = 4;
+constexpr int kTwoPhaseThreads = (kWarpsPerCta + 1 + kPreparers) * 32;
+static_assert(kStages % kPreparers == 0, "each stage must always go to the same preparer");
+
 template <typename T, bool VCS>
 struct TwoPhaseSmem {
   static constexpr int kPipe = 0;
   static constexpr int kRecs = PipeLayout<T, VCS>::kExtra;
   static constexpr int kPrep = kRecs + kStages * RecLayout<T>::kBytes;
-  static constexpr int kQueue = kPrep + PrepLayout::kBytes;
+  static constexpr int kQueue = kPrep + kPreparers * PrepLayout::kBytes;
   static constexpr int kTile =
       kQueue + ((kWarpsPerCta * kQueueCap * (8 + (int)sizeof(T)) + 127) / 128 * 128);
 };
@@ -352,37 +362,43 @@ struct TwoPhaseWarp {
     }
   }
 
-  // Applies, in record order, the records [0, nrec) whose row lies in this
-  // warp's band [lo, hi) of the tile.
+  // Applies, in record order, the records [0, nrec) whose tile row this warp
+  // owns: rows t with t mod kWarpsPerCta == owner (interleaved, so that the
+  // popular rows of a skewed matrix spread over the warps).  Owned records are
+  // compacted into the warp's queue in order; whenever it holds a warp's worth
+  // they are applied E at a time (whole steps), the rest kept for later.
   __device__ __forceinline__ static void run(const uint32_t *key, const T *val, int nrec, int s0,
                                              const T *__restrict__ X, int64_t ldx, T *tile, int w,
-                                             int lo, int hi, uint32_t *qkey, T *qval,
+                                             int owner, uint32_t *qkey, T *qval,
                                              const int (&col0)[CI], const bool (&colok)[CI]) {
     const int lane = threadIdx.x & 31, grp = lane / Q;
     const unsigned lt = lanemask_lt();
+    int qn = 0;  // records waiting in the queue (< 32 between chunks)
     for (int base = 0; base < nrec; base += 32) {
       const int r = base + lane;
       uint32_t kk = 0;
       bool in = false;
       if (r < nrec) {
         kk = key[r];
-        const int t = (int)(kk & 0xffffu);
-        in = t >= lo && t < hi;
+        in = ((int)(kk & 0xffffu) & (kWarpsPerCta - 1)) == owner;
       }
       const unsigned m = __ballot_sync(kFullMask, in);
-      if (in) {  // compact the in-band records into the warp's queue, in order
-        const int p = __popc(m & lt);
+      if (in) {
+        const int p = qn + __popc(m & lt);
         qkey[p] = kk;
         qval[p] = val[r];
       }
+      qn += __popc(m);
+      const bool last = base + 32 >= nrec;
+      if (qn < 32 && !last) continue;
       __syncwarp();
-      const int cnt = __popc(m);
-      for (int c0 = 0; c0 < cnt; c0 += E) {
+      const int upto = last ? qn : qn - qn % E;  // whole steps now, all at the end
+      for (int c0 = 0; c0 < upto; c0 += E) {
         const int qi = c0 + grp;
         int tk = -1;
         T ak = T(0);
         T x[CI][VEC];
-        if (qi < cnt) {
+        if (qi < upto) {
           const uint32_t q = qkey[qi];
           tk = (int)(q & 0xffffu);
           ak = qval[qi];
@@ -400,22 +416,38 @@ struct TwoPhaseWarp {
         } else {
           // equal rows inside the step: one round per earlier duplicate, in record order
           const int rank = __popc(peers & lt) / Q;
-          for (int rd = 0; rd < E; ++rd) {
+          const int rounds = (int)__reduce_max_sync(kFullMask, tk >= 0 ? (unsigned)rank : 0u) + 1;
+          for (int rd = 0; rd < rounds; ++rd) {
             if (tk >= 0 && rank == rd) apply(tile, w, tk, ak, x, col0, colok);
             __syncwarp();
           }
         }
       }
+      // keep the unapplied tail (fewer than E records) at the front, in order
       __syncwarp();
+      uint32_t tk2 = 0;
+      T tv = T(0);
+      const int rest = qn - upto;
+      if (lane < rest) {
+        tk2 = qkey[upto + lane];
+        tv = qval[upto + lane];
+      }
+      __syncwarp();
+      if (lane < rest) {
+        qkey[lane] = tk2;
+        qval[lane] = tv;
+      }
+      __syncwarp();
+      qn = rest;
     }
   }
 };
 
 // Block (tile blockIdx.x, group blockIdx.y).  The producer warp streams the
 // group's blocks and turns each into the records of this tile; consumer warp w
-// applies the records of its band of the tile's rows.
+// applies the records of the tile rows it owns.
 template <typename T, int VEC, int Q, int CI, bool VCS>
-__global__ void __launch_bounds__(kPipeThreads) two_phase_kernel(const TwoPhaseArgs a) {
+__global__ void __launch_bounds__(kTwoPhaseThreads) two_phase_kernel(const TwoPhaseArgs a) {
   using WP = TwoPhaseWarp<T, VEC, Q, CI, VCS>;
   using SM = TwoPhaseSmem<T, VCS>;
   using RL = RecLayout<T>;
@@ -430,41 +462,23 @@ __global__ void __launch_bounds__(kPipeThreads) two_phase_kernel(const TwoPhaseA
   const int rows = (int)(a.n_t - t0 < a.tile_rows ? a.n_t - t0 : a.tile_rows);
   const int w = a.w;
   const int b_lo = a.bounds[blockIdx.y], b_hi = a.bounds[blockIdx.y + 1];
-  for (int q = threadIdx.x; q < rows * w; q += kPipeThreads) tile[q] = T(0);
+  for (int q = threadIdx.x; q < rows * w; q += blockDim.x) tile[q] = T(0);
   pipe.init();  // (its barrier also publishes the zeroed tile)
   if (wid == kWarpsPerCta) {
-    // ---- producer: issue block i, then prepare block i - 1
+    // ---- issuing warp: every block of the group, in order
+    pipe.issue_all(a.st, b_lo, b_hi, 1);
+  } else if (wid > kWarpsPerCta) {
+    // ---- preparing warp e: blocks e, e + kPreparers, ... as they land
+    const int e = wid - kWarpsPerCta - 1;
     const bool search = VCS && a.sorted && rows < a.n_t;
-    int i = 0, done = 0;
-    bool ok = true;
-    DescWindow win;
-    for (int b = b_lo; b < b_hi; ++b, ++i) {
-      const int st = i % kStages;
-      if (i >= kStages && !mbar_wait_bounded(pipe.empty(st), ((i / kStages) - 1) & 1, kWaitLimitNs)) {
-        ok = false;
+    for (int i = e; i < b_hi - b_lo; i += kPreparers)
+      if (*reinterpret_cast<volatile int *>(pipe.fail()) ||
+          !two_phase_prepare<T, VCS>(pipe, a.st, i, b_lo + i, recs, prep + e * PrepLayout::kBytes,
+                                     t0, rows, search)) {
+        pipe.give_up(a.st);
         break;
       }
-      int4 d[3];
-      win.get(a.st.blocks, b_lo, 1, b_hi, i, d);
-      if (lane == 0) stage_issue<T, VCS>(a.st, d, pipe.buf(st), pipe.full(st));
-      __syncwarp();
-      for (; done < i; ++done)
-        if (!two_phase_prepare<T, VCS>(pipe, a.st, done, b_lo + done, recs, prep, t0, rows, search)) {
-          ok = false;
-          break;
-        }
-      if (!ok) break;
-    }
-    for (; ok && done < i; ++done)
-      if (!two_phase_prepare<T, VCS>(pipe, a.st, done, b_lo + done, recs, prep, t0, rows, search))
-        ok = false;
-    if (!ok) pipe.give_up(a.st);
-    if (lane == 0)
-      for (int j = i - kStages < 0 ? 0 : i - kStages; j < i; ++j)
-        mbar_wait_bounded(pipe.full(j % kStages), (j / kStages) & 1, kWaitLimitNs);
   } else {
-    const int band = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
-    const int lo = min(rows, wid * band), hi = min(rows, lo + band);
     const int ql = lane & (Q - 1);
     int col0[CI];
     bool colok[CI];
@@ -486,11 +500,10 @@ __global__ void __launch_bounds__(kPipeThreads) two_phase_kernel(const TwoPhaseA
       }
       const Block k = stage_desc<T, VCS>(pipe.buf(st));
       const unsigned char *rb = recs + st * RL::kBytes;
-      if (lo < hi)
-        WP::run(reinterpret_cast<const uint32_t *>(rb + RL::kKey),
-                reinterpret_cast<const T *>(rb + RL::kVal),
-                *reinterpret_cast<const int *>(rb + RL::kCount), k.s0, X, a.ldx, tile, w, lo, hi,
-                qkey, qval, col0, colok);
+      WP::run(reinterpret_cast<const uint32_t *>(rb + RL::kKey),
+              reinterpret_cast<const T *>(rb + RL::kVal),
+              *reinterpret_cast<const int *>(rb + RL::kCount), k.s0, X, a.ldx, tile, w, wid,
+              qkey, qval, col0, colok);
       pipe.release(i);
     }
   }
@@ -498,7 +511,7 @@ __global__ void __launch_bounds__(kPipeThreads) two_phase_kernel(const TwoPhaseA
   if (*pipe.fail()) return;
   // the tile: final Y when C == 1, else this group's partial
   T *__restrict__ out = static_cast<T *>(a.out) + (int64_t)blockIdx.y * a.part_stride;
-  for (int q = threadIdx.x; q < rows * w; q += kPipeThreads) {
+  for (int q = threadIdx.x; q < rows * w; q += blockDim.x) {
     const int rr = q / w, c = q - rr * w;
     out[(t0 + rr) * a.ldo + c] = tile[q];
   }
@@ -651,7 +664,7 @@ vs_status two_phase_typed(vs_handle_s &h, const Matrix &m, DenseView X, DenseVie
     const int64_t tiles = (n_t + tile_rows - 1) / tile_rows;
     const size_t smem = stage + (size_t)tile_rows * row_bytes;
     int resident = 0;  // (raises the kernel's shared-memory limit once)
-    VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(k), kPipeThreads, (int)smem, &resident));
+    VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(k), kTwoPhaseThreads, (int)smem, &resident));
     TwoPhaseArgs a;
     a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
                        xp, X.ld, (int)sizeof(T), wb};
@@ -673,7 +686,7 @@ vs_status two_phase_typed(vs_handle_s &h, const Matrix &m, DenseView X, DenseVie
       a.part_stride = n_t * wb;
     }
     dim3 grid((unsigned)tiles, (unsigned)C);
-    k<<<grid, kPipeThreads, smem, s>>>(a);
+    k<<<grid, kTwoPhaseThreads, smem, s>>>(a);
     VS_LAUNCH_CHECK();
     if (C > 1) {
       const int64_t total = n_t * wb;
@@ -760,7 +773,7 @@ vs_status two_phase_static_typed(const Matrix &m, DenseView X, DenseView Y, int6
     const int64_t tiles = (n_t + tile_rows - 1) / tile_rows;
     const size_t smem = stage + (size_t)tile_rows * row_bytes;
     int resident = 0;  // (raises the kernel's shared-memory limit once)
-    VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(k), kPipeThreads, (int)smem, &resident));
+    VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(k), kTwoPhaseThreads, (int)smem, &resident));
     TwoPhaseArgs a;
     a.st = StageArrays{m.ptr, m.idx, m.vals, m.vptr, m.blocks, (int)m.n_blocks, m.err,
                        xp, X.ld, (int)sizeof(T), wb};
@@ -781,7 +794,7 @@ vs_status two_phase_static_typed(const Matrix &m, DenseView X, DenseView Y, int6
       a.part_stride = n_t * wb;
     }
     dim3 grid((unsigned)tiles, (unsigned)C);
-    k<<<grid, kPipeThreads, smem, s>>>(a);
+    k<<<grid, kTwoPhaseThreads, smem, s>>>(a);
     VS_LAUNCH_CHECK();
     if (C > 1) {
       const int64_t total = n_t * wb;
