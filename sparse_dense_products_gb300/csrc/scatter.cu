@@ -177,8 +177,9 @@ template <typename T>
 struct RecLayout {
   static constexpr int kKey = 0;
   static constexpr int kVal = kKey + kCapEntries * 4;
-  static constexpr int kCount = kVal + kCapEntries * (int)sizeof(T);
-  static constexpr int kBytes = (kCount + 16 + 127) / 128 * 128;
+  // records sorted by owning warp: warp w's are [kOff[w], kOff[w + 1])
+  static constexpr int kOff = kVal + kCapEntries * (int)sizeof(T);
+  static constexpr int kBytes = (kOff + 4 * (kWarpsPerCta + 1) + 127) / 128 * 128;
 };
 
 // Producer-side scratch (one per CTA): start bitmaps of slices and runs, and
@@ -188,10 +189,11 @@ struct PrepLayout {
   static constexpr int kSliceBits = 0;
   static constexpr int kRunBits = kSliceBits + kWords * 4;
   static constexpr int kSliceIds = kRunBits + kWords * 4;
-  static constexpr int kBytes = (kSliceIds + kCapSlices * 4 + 127) / 128 * 128;
+  static constexpr int kCursor = kSliceIds + kCapSlices * 4;           // per owning warp
+  static constexpr int kRange = kCursor + 4 * kWarpsPerCta;            // per run: [a0, b0)
+  static constexpr int kBytes = (kRange + 8 * kCapRuns + 127) / 128 * 128;
 };
 
-constexpr int kQueueCap = 64;  // per-warp queue of in-band records
 
 // Two-phase CTA: kWarpsPerCta consumer warps, one warp issuing the copies and
 // kPreparers warps turning landed blocks into records (block i goes to
@@ -206,9 +208,7 @@ struct TwoPhaseSmem {
   static constexpr int kPipe = 0;
   static constexpr int kRecs = PipeLayout<T, VCS>::kExtra;
   static constexpr int kPrep = kRecs + kStages * RecLayout<T>::kBytes;
-  static constexpr int kQueue = kPrep + kPreparers * PrepLayout::kBytes;
-  static constexpr int kTile =
-      kQueue + ((kWarpsPerCta * kQueueCap * (8 + (int)sizeof(T)) + 127) / 128 * 128);
+  static constexpr int kTile = kPrep + kPreparers * PrepLayout::kBytes;
 };
 
 // Producer warp: once block j (number b) has landed, write the records of its
@@ -235,19 +235,22 @@ __device__ __forceinline__ bool two_phase_prepare(const Pipe<T, VCS> &pipe, cons
   unsigned char *rb = recs + s * RL::kBytes;
   uint32_t *key = reinterpret_cast<uint32_t *>(rb + RL::kKey);
   T *val = reinterpret_cast<T *>(rb + RL::kVal);
-  int *count = reinterpret_cast<int *>(rb + RL::kCount);
+  int *off = reinterpret_cast<int *>(rb + RL::kOff);
   uint32_t *sbm = reinterpret_cast<uint32_t *>(prep + PrepLayout::kSliceBits);
   uint32_t *rbm = reinterpret_cast<uint32_t *>(prep + PrepLayout::kRunBits);
   int32_t *sid = reinterpret_cast<int32_t *>(prep + PrepLayout::kSliceIds);
+  int *cur = reinterpret_cast<int *>(prep + PrepLayout::kCursor);
+  int *rng = reinterpret_cast<int *>(prep + PrepLayout::kRange);
   const int eb = align_down<4>(k.e0);
   const int nwords = (k.e1 - eb + 31) / 32;
-  int nrec = 0;
+  constexpr int kOwnMask = kWarpsPerCta - 1;
 
   // slice and run start bitmaps over the block's entries
   for (int q = lane; q < nwords; q += 32) {
     sbm[q] = 0u;
     if (VCS) rbm[q] = 0u;
   }
+  if (lane < kWarpsPerCta) cur[lane] = 0;
   __syncwarp();
   int ns = 0;  // non-empty slices, in order
   if (k.type == 0) {
@@ -279,64 +282,119 @@ __device__ __forceinline__ bool two_phase_prepare(const Pipe<T, VCS> &pipe, cons
   }
   __syncwarp();
 
-  if (!(VCS && skip_by_search)) {
-    // every entry of the block, 32 at a time
-    int sbase = -1, rbase = k.r0 - 1;
-    for (int q = 0; q < nwords; ++q) {
-      const int n = eb + 32 * q + lane;
-      const uint32_t sw = sbm[q];
-      const uint32_t rw = VCS ? rbm[q] : 0u;
-      const int sidx = sbase + __popc(sw & le);
-      const int ridx = rbase + __popc(rw & le);
-      sbase += __popc(sw);
-      rbase += __popc(rw);
-      bool in = false;
-      int tt = 0;
-      if (n >= k.e0 && n < k.e1) {
-        tt = (int)(sv.idx[n] - t0);
-        in = tt >= 0 && tt < rows;
-      }
-      const unsigned m = __ballot_sync(kFullMask, in);
+  // The records are sorted by owning warp (tile row mod kWarpsPerCta), stably:
+  // pass 0 counts each warp's records, pass 1 places each record at its
+  // warp's cursor.  Within a warp's list the order is the entries' order.
+  // `emit` takes one candidate entry per lane (the same on both passes).
+  auto emit = [&](int pass, bool in, int tt, uint32_t kk, T vv) {
+    const int own = tt & kOwnMask;
+    const unsigned peers = __match_any_sync(kFullMask, in ? own : -1);
+    const int rank = __popc(peers & lt);
+    if (pass == 0) {
+      if (in && rank == 0) atomicAdd(&cur[own], __popc(peers));
+    } else {
       if (in) {
-        const int pos = nrec + __popc(m & lt);
-        key[pos] = (uint32_t)tt | ((uint32_t)sid[sidx] << 16);
-        val[pos] = VCS ? (T)rv[ridx] : sv.vals[n];
+        const int pos = cur[own] + rank;
+        key[pos] = kk;
+        val[pos] = vv;
       }
-      nrec += __popc(m);
+      __syncwarp();
+      if (in && rank == 0) cur[own] += __popc(peers);
+      __syncwarp();
     }
-  } else {
-    // sorted runs, partial tile: per run, only the entries inside [t0, t0 + rows)
-    int cur_slice = 0;  // index into sid
-    for (int r = k.r0; r < k.r1; ++r) {
-      int lo = max(sv.vptr[r], k.e0), hi = min(sv.vptr[r + 1], k.e1);
-      while (cur_slice + 1 < ns) {  // the slice holding run r's first entry
-        const int nxt = k.type == 0 ? sv.vptr[sv.ptr[k.s0 + sid[cur_slice + 1]]] : k.e1;
-        if (nxt <= lo) ++cur_slice;
-        else break;
+  };
+  for (int pass = 0; pass < 2; ++pass) {
+    if (!(VCS && skip_by_search)) {
+      // every entry of the block, 32 at a time (pass 0 needs only the rows)
+      int sbase = -1, rbase = k.r0 - 1;
+      for (int q = 0; q < nwords; ++q) {
+        const int n = eb + 32 * q + lane;
+        bool in = false;
+        int tt = 0;
+        if (n >= k.e0 && n < k.e1) {
+          tt = (int)(sv.idx[n] - t0);
+          in = tt >= 0 && tt < rows;
+        }
+        uint32_t kk = 0;
+        T vv = T(0);
+        if (pass == 1) {
+          const uint32_t sw = sbm[q];
+          const uint32_t rw = VCS ? rbm[q] : 0u;
+          const int sidx = sbase + __popc(sw & le);
+          const int ridx = rbase + __popc(rw & le);
+          sbase += __popc(sw);
+          rbase += __popc(rw);
+          if (in) {
+            kk = (uint32_t)tt | ((uint32_t)sid[sidx] << 16);
+            vv = VCS ? (T)rv[ridx] : sv.vals[n];
+          }
+        }
+        emit(pass, in, tt, kk, vv);
       }
-      // first entry with row >= t0, then first with row >= t0 + rows
-      int a0 = lo, a1 = hi;
-      while (a0 < a1) {
-        const int mid = (a0 + a1) >> 1;
-        if (sv.idx[mid] < t0) a0 = mid + 1;
-        else a1 = mid;
+    } else {
+      // sorted runs, partial tile: per run, only the entries inside [t0, t0 + rows)
+      int cur_slice = 0;  // index into sid
+      for (int r = k.r0; r < k.r1; ++r) {
+        int a0, b0;
+        if (pass == 0) {
+          const int lo = max(sv.vptr[r], k.e0), hi = min(sv.vptr[r + 1], k.e1);
+          // first entry with row >= t0, then first with row >= t0 + rows
+          int x0 = lo, x1 = hi;
+          while (x0 < x1) {
+            const int mid = (x0 + x1) >> 1;
+            if (sv.idx[mid] < t0) x0 = mid + 1;
+            else x1 = mid;
+          }
+          int y0 = x0, y1 = hi;
+          while (y0 < y1) {
+            const int mid = (y0 + y1) >> 1;
+            if (sv.idx[mid] < t0 + rows) y0 = mid + 1;
+            else y1 = mid;
+          }
+          a0 = x0;
+          b0 = y0;
+          if (lane == 0) {
+            rng[2 * (r - k.r0)] = a0;
+            rng[2 * (r - k.r0) + 1] = b0;
+          }
+        } else {
+          a0 = rng[2 * (r - k.r0)];
+          b0 = rng[2 * (r - k.r0) + 1];
+        }
+        while (cur_slice + 1 < ns) {  // the slice holding run r's first entry
+          const int nxt = k.type == 0 ? sv.vptr[sv.ptr[k.s0 + sid[cur_slice + 1]]] : k.e1;
+          if (nxt <= max(sv.vptr[r], k.e0)) ++cur_slice;
+          else break;
+        }
+        const uint32_t sk = (uint32_t)sid[cur_slice] << 16;
+        const T v = (T)rv[r];
+        for (int base = a0; base < b0; base += 32) {
+          const int n = base + lane;
+          const bool in = n < b0;
+          const int tt = in ? (int)(sv.idx[n] - t0) : 0;
+          emit(pass, in, tt, (uint32_t)tt | sk, v);
+        }
       }
-      int b0 = a0, b1 = hi;
-      while (b0 < b1) {
-        const int mid = (b0 + b1) >> 1;
-        if (sv.idx[mid] < t0 + rows) b0 = mid + 1;
-        else b1 = mid;
+    }
+    __syncwarp();
+    if (pass == 0) {
+      // counts -> offsets (exclusive scan over the owning warps) and cursors
+      const int c = lane < kWarpsPerCta ? cur[lane] : 0;
+      int incl = c;
+#pragma unroll
+      for (int d = 1; d < kWarpsPerCta; d <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, incl, d);
+        if (lane >= d) incl += y;
       }
-      const uint32_t sk = (uint32_t)sid[cur_slice] << 16;
-      const T v = (T)rv[r];
-      for (int n = a0 + lane; n < b0; n += 32) {
-        key[nrec + n - a0] = (uint32_t)(sv.idx[n] - t0) | sk;
-        val[nrec + n - a0] = v;
+      __syncwarp();
+      if (lane < kWarpsPerCta) {
+        off[lane] = incl - c;
+        cur[lane] = incl - c;
       }
-      nrec += b0 - a0;
+      if (lane == kWarpsPerCta - 1) off[kWarpsPerCta] = incl;
+      __syncwarp();
     }
   }
-  if (lane == 0) *count = nrec;
   __syncwarp();
   if (lane == 0) mbar_arrive(pipe.ready(s));
   return true;
@@ -362,83 +420,58 @@ struct TwoPhaseWarp {
     }
   }
 
-  // Applies, in record order, the records [0, nrec) whose tile row this warp
-  // owns: rows t with t mod kWarpsPerCta == owner (interleaved, so that the
-  // popular rows of a skewed matrix spread over the warps).  Owned records are
-  // compacted into the warp's queue in order; whenever it holds a warp's worth
-  // they are applied E at a time (whole steps), the rest kept for later.
-  __device__ __forceinline__ static void run(const uint32_t *key, const T *val, int nrec, int s0,
-                                             const T *__restrict__ X, int64_t ldx, T *tile, int w,
-                                             int owner, uint32_t *qkey, T *qval,
-                                             const int (&col0)[CI], const bool (&colok)[CI]) {
+  // Applies, in record order, this warp's records [lo, hi) of a block: those
+  // whose tile row t has t mod kWarpsPerCta == the warp's number (rows
+  // interleaved over the warps, so that the popular rows of a skewed matrix
+  // spread out), E records per step.
+  __device__ __forceinline__ static void run(const uint32_t *key, const T *val, int lo, int hi,
+                                             int s0, const T *__restrict__ X, int64_t ldx, T *tile,
+                                             int w, const int (&col0)[CI],
+                                             const bool (&colok)[CI]) {
     const int lane = threadIdx.x & 31, grp = lane / Q;
     const unsigned lt = lanemask_lt();
-    int qn = 0;  // records waiting in the queue (< 32 between chunks)
-    for (int base = 0; base < nrec; base += 32) {
-      const int r = base + lane;
-      uint32_t kk = 0;
-      bool in = false;
-      if (r < nrec) {
-        kk = key[r];
-        in = ((int)(kk & 0xffffu) & (kWarpsPerCta - 1)) == owner;
-      }
-      const unsigned m = __ballot_sync(kFullMask, in);
-      if (in) {
-        const int p = qn + __popc(m & lt);
-        qkey[p] = kk;
-        qval[p] = val[r];
-      }
-      qn += __popc(m);
-      const bool last = base + 32 >= nrec;
-      if (qn < 32 && !last) continue;
-      __syncwarp();
-      const int upto = last ? qn : qn - qn % E;  // whole steps now, all at the end
-      for (int c0 = 0; c0 < upto; c0 += E) {
-        const int qi = c0 + grp;
-        int tk = -1;
-        T ak = T(0);
-        T x[CI][VEC];
-        if (qi < upto) {
-          const uint32_t q = qkey[qi];
-          tk = (int)(q & 0xffffu);
-          ak = qval[qi];
-          const int sl = s0 + (int)(q >> 16);
+    // one step's record: row, value and the X row of its slice
+    auto load = [&](int c0, int &tk, T &ak, T (&x)[CI][VEC]) {
+      const int qi = c0 + grp;
+      tk = -1;
+      ak = T(0);
+      if (qi < hi) {
+        const uint32_t q = key[qi];
+        tk = (int)(q & 0xffffu);
+        ak = val[qi];
+        const int sl = s0 + (int)(q >> 16);
 #pragma unroll
-          for (int ci = 0; ci < CI; ++ci)
-            if (colok[ci])
-              Ops::unpack(ld_gather(reinterpret_cast<const V *>(X + (int64_t)sl * ldx + col0[ci])),
-                          x[ci]);
+        for (int ci = 0; ci < CI; ++ci)
+          if (colok[ci])
+            Ops::unpack(ld_gather(reinterpret_cast<const V *>(X + (int64_t)sl * ldx + col0[ci])),
+                        x[ci]);
+      }
+    };
+    int tn;
+    T an, xn[CI][VEC];
+    if (lo < hi) load(lo, tn, an, xn);
+    for (int c0 = lo; c0 < hi; c0 += E) {
+      const int tk = tn;
+      const T ak = an;
+      T x[CI][VEC];
+#pragma unroll
+      for (int ci = 0; ci < CI; ++ci)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) x[ci][e] = xn[ci][e];
+      if (c0 + E < hi) load(c0 + E, tn, an, xn);  // the next step's loads overlap this step
+      const unsigned peers = __match_any_sync(kFullMask, tk);
+      const bool dup = tk >= 0 && __popc(peers) > Q;
+      if (!__any_sync(kFullMask, dup)) {
+        if (tk >= 0) apply(tile, w, tk, ak, x, col0, colok);
+      } else {
+        // equal rows inside the step: one round per earlier duplicate, in record order
+        const int rank = __popc(peers & lt) / Q;
+        const int rounds = (int)__reduce_max_sync(kFullMask, tk >= 0 ? (unsigned)rank : 0u) + 1;
+        for (int rd = 0; rd < rounds; ++rd) {
+          if (tk >= 0 && rank == rd) apply(tile, w, tk, ak, x, col0, colok);
+          __syncwarp();
         }
-        const unsigned peers = __match_any_sync(kFullMask, tk);
-        const bool dup = tk >= 0 && __popc(peers) > Q;
-        if (!__any_sync(kFullMask, dup)) {
-          if (tk >= 0) apply(tile, w, tk, ak, x, col0, colok);
-        } else {
-          // equal rows inside the step: one round per earlier duplicate, in record order
-          const int rank = __popc(peers & lt) / Q;
-          const int rounds = (int)__reduce_max_sync(kFullMask, tk >= 0 ? (unsigned)rank : 0u) + 1;
-          for (int rd = 0; rd < rounds; ++rd) {
-            if (tk >= 0 && rank == rd) apply(tile, w, tk, ak, x, col0, colok);
-            __syncwarp();
-          }
-        }
       }
-      // keep the unapplied tail (fewer than E records) at the front, in order
-      __syncwarp();
-      uint32_t tk2 = 0;
-      T tv = T(0);
-      const int rest = qn - upto;
-      if (lane < rest) {
-        tk2 = qkey[upto + lane];
-        tv = qval[upto + lane];
-      }
-      __syncwarp();
-      if (lane < rest) {
-        qkey[lane] = tk2;
-        qval[lane] = tv;
-      }
-      __syncwarp();
-      qn = rest;
     }
   }
 };
@@ -488,9 +521,6 @@ __global__ void __launch_bounds__(kTwoPhaseThreads) two_phase_kernel(const TwoPh
       colok[ci] = col0[ci] < w;
     }
     const T *__restrict__ X = static_cast<const T *>(a.X);
-    unsigned char *qbase = smem + SM::kQueue + wid * kQueueCap * (8 + (int)sizeof(T));
-    uint32_t *qkey = reinterpret_cast<uint32_t *>(qbase);
-    T *qval = reinterpret_cast<T *>(qbase + kQueueCap * 8);
     int i = 0;
     for (int b = b_lo; b < b_hi; ++b, ++i) {
       const int st = i % kStages;
@@ -500,10 +530,10 @@ __global__ void __launch_bounds__(kTwoPhaseThreads) two_phase_kernel(const TwoPh
       }
       const Block k = stage_desc<T, VCS>(pipe.buf(st));
       const unsigned char *rb = recs + st * RL::kBytes;
+      const int *off = reinterpret_cast<const int *>(rb + RL::kOff);
       WP::run(reinterpret_cast<const uint32_t *>(rb + RL::kKey),
-              reinterpret_cast<const T *>(rb + RL::kVal),
-              *reinterpret_cast<const int *>(rb + RL::kCount), k.s0, X, a.ldx, tile, w, wid,
-              qkey, qval, col0, colok);
+              reinterpret_cast<const T *>(rb + RL::kVal), off[wid], off[wid + 1], k.s0, X, a.ldx,
+              tile, w, col0, colok);
       pipe.release(i);
     }
   }
@@ -526,8 +556,18 @@ __global__ void combine_kernel(const T *__restrict__ P, int C, int64_t part_stri
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = i / w;
     const int c = (int)(i - t * w);
+    // the partials in group order, kBatch loads in flight before their adds
+    constexpr int kBatch = 8;
     T sum = P[i];
-    for (int k = 1; k < C; ++k) sum = sum + P[(int64_t)k * part_stride + i];
+    for (int k0 = 1; k0 < C; k0 += kBatch) {
+      T v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        v[j] = k0 + j < C ? P[(int64_t)(k0 + j) * part_stride + i] : T(0);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if (k0 + j < C) sum = sum + v[j];
+    }
     Y[t * ldy + c] = sum;
   }
 }
