@@ -441,6 +441,15 @@ def gpu_arm(args):
         torch.cuda.synchronize()
         l2_warm[p[0]] = round(statistics.median(a.elapsed_time(b) for a, b in evs), 5)
 
+    # ---- the gather floor of each product (vs_gather_floor: the same index
+    # stream and operand rows, nothing else), the second roof made concrete
+    floor_ms = {}
+    for name, layout, major, direction in PRODUCTS:
+        B = Bab if direction == "A@B" else Bt.t()
+        A = handles[(layout, major)]
+        ts = timed(lambda: vs.gather_floor(A, B, direction), max(5, args.steps))
+        floor_ms[name] = round(statistics.median(ts), 5)
+
     # ---- host cost of one asynchronous vs_spmm call (enqueue only)
     torch.cuda.synchronize()
     n_calls = 200
@@ -495,7 +504,9 @@ def gpu_arm(args):
     onchip = {"bound": "l1/shared gather", "kernel": dom, "achieved": round(onchip_ach, 1),
               "peak": round(onchip_peak, 1), "peak_kind": "nominal: 128 B/clk/SM x SMs x sampled SM clock",
               "unit": "GB/s", "frac": round(onchip_ach / onchip_peak, 4),
-              "bytes_per_launch": onchip_bytes}
+              "bytes_per_launch": onchip_bytes,
+              "gather_floor_ms": floor_ms[dom],
+              "product_over_floor": round(ms_prod[dom] / floor_ms[dom], 3)}
 
     # ---- CPU baseline: the float64 oracle on host cores (rank 0, N=1 only)
     cpu = None
@@ -535,6 +546,7 @@ def gpu_arm(args):
         "products": products,
         "misaligned_variants": variants,
         "products_l2_warm_ms": l2_warm,
+        "gather_floor_ms": floor_ms,
         "cusparse": cusparse,
         "assembly_ms": assembly,
         "wall_s_timed_region": round(wall, 3),

@@ -336,6 +336,21 @@ int32_t vs_version(void);
  * all handles); a benchmark reads it before and after a timed region. */
 int64_t vs_kernel_launches(void);
 
+/*
+ * vs_gather_floor -- a measurement, not a product: the memory-side floor of
+ * the gather that vs_spmm(A, B, dir, VS_DETERMINISTIC) runs.  One kernel
+ * reads every stored index of the matrix that product walks (the attached
+ * transpose for a misaligned direction, when there is one) in storage order,
+ * loads the row of B it names through L1 with 16-byte loads and adds the rows
+ * into registers; no values, no summation tree, no pipeline, no output rows.
+ * Its time is what fetching the operand rows alone costs for this matrix's
+ * index stream, the second roof beside HBM.  The sums go to handle scratch.
+ * Needs a float32 B whose width is a multiple of 4 and at most 64, with the
+ * layout rules of vs_spmm, and for a misaligned direction an attached
+ * transpose (VS_ERR_UNSUPPORTED otherwise).
+ */
+vs_status vs_gather_floor(vs_handle A, const vs_dense *B, vs_direction dir, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,9 +5,9 @@ csrc/); this package is its thin Python binding.  Importing the package does
 not load the library; the first call does, and fails loudly when libvs has not
 been built (``python -m sparse_dense_products_gb300.build``).
 """
-from .api import (SparseMatrix, build_csr, build_vcs, empty_out, kernel_launches,  # noqa: F401
-                  spmm, spmm_host, version)
+from .api import (SparseMatrix, build_csr, build_vcs, empty_out, gather_floor,  # noqa: F401
+                  kernel_launches, spmm, spmm_host, version)
 from ._lib import VsError  # noqa: F401
 
-__all__ = ["SparseMatrix", "build_csr", "build_vcs", "empty_out", "kernel_launches", "spmm",
-           "spmm_host", "version", "VsError"]
+__all__ = ["SparseMatrix", "build_csr", "build_vcs", "empty_out", "gather_floor",
+           "kernel_launches", "spmm", "spmm_host", "version", "VsError"]

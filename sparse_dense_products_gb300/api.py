@@ -261,6 +261,15 @@ def spmm_host(A: SparseMatrix, B: torch.Tensor, direction: str = "A@B",
     return out
 
 
+def gather_floor(A: SparseMatrix, B: torch.Tensor, direction: str = "A@B") -> None:
+    """``vs_gather_floor``: enqueue the gather-only measurement kernel for the
+    product ``spmm(A, B, direction)`` (time it with CUDA events)."""
+    _require_cuda(B)
+    bd = _dense(B)
+    L.check(L.load().vs_gather_floor(A.handle, ctypes.byref(bd), _DIRS[direction],
+                                     ctypes.c_void_p(_stream_ptr(B.device))))
+
+
 def version() -> int:
     return int(L.load().vs_version())
 

@@ -295,6 +295,47 @@ __global__ void scale_rows_kernel(const T *X, int64_t rows, int64_t ldx, int64_t
     out[r * ldo + c] = X[r * ldx + c] * s[r];
   }
 }
+
+// The gather floor: entries in storage order, Q = w / 4 lanes per entry, each
+// loading 16 bytes of the entry's operand row; U entries per lane in flight.
+template <int U>
+__global__ void __launch_bounds__(256) gather_floor_kernel(const int32_t *__restrict__ idx,
+                                                          int64_t nnz, const float4 *__restrict__ X,
+                                                          int64_t ldx4, int q, float *sink) {
+  const int lane = threadIdx.x & 31;
+  const int per = 32 / q;  // entries per warp step
+  const int ql = lane % q, slot = lane / q;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (slot < per) {
+    const int64_t stride = nwarps * per;
+    int64_t n = warp * per + slot;
+    for (; n + (U - 1) * stride < nnz; n += U * stride) {
+      int j[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) j[u] = __ldg(idx + n + u * stride);
+      float4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) x[u] = __ldg(X + (size_t)(uint32_t)j[u] * ldx4 + ql);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        acc.x += x[u].x;
+        acc.y += x[u].y;
+        acc.z += x[u].z;
+        acc.w += x[u].w;
+      }
+    }
+    for (; n < nnz; n += stride) {
+      const float4 x = __ldg(X + (size_t)(uint32_t)__ldg(idx + n) * ldx4 + ql);
+      acc.x += x.x;
+      acc.y += x.y;
+      acc.z += x.z;
+      acc.w += x.w;
+    }
+  }
+  sink[(int64_t)blockIdx.x * blockDim.x + threadIdx.x] = acc.x + acc.y + acc.z + acc.w;
+}
 }  // namespace vs_derive
 
 namespace vs {
@@ -598,6 +639,49 @@ vs_status vs_scale_entries(vs_handle A, const void *factors, cudaStream_t stream
   return VS_OK;
 }
 
+vs_status vs_gather_floor(vs_handle A, const vs_dense *B, vs_direction dir, cudaStream_t stream) {
+  if (!valid_handle(A)) return invalid("NULL handle");
+  if (!B) return invalid("NULL operand descriptor");
+  if (dir != VS_A_B && dir != VS_B_A) return invalid("unknown direction");
+  // B in the slice frame, as vs_spmm would read it (width axis contiguous)
+  const bool ab = dir == VS_A_B;
+  const int64_t w = ab ? B->cols : B->rows;
+  const int64_t rows = ab ? B->rows : B->cols;
+  const int64_t ld = ab ? (B->rows > 1 ? B->row_stride : w) : (B->cols > 1 ? B->col_stride : w);
+  if (rows != (ab ? A->A.n_cols : A->A.n_rows)) {
+    set_error("B does not match the matrix for this direction");
+    return VS_ERR_SHAPE;
+  }
+  if (w > 1 && (ab ? B->col_stride : B->row_stride) != 1) {
+    set_error("the width axis of B must have stride 1");
+    return VS_ERR_LAYOUT;
+  }
+  const DenseView X{B->ptr, rows, ld};
+  const bool aligned = ab == (A->A.major == VS_MAJOR_ROW);
+  if (B->dtype != VS_F32 || w % 4 != 0 || w > 64 || (reinterpret_cast<uintptr_t>(X.p) % 16) ||
+      X.ld % 4 != 0) {
+    set_error("vs_gather_floor needs float32 16-byte-aligned rows, width a multiple of 4 up to 64");
+    return VS_ERR_UNSUPPORTED;
+  }
+  if (!aligned && !A->T) {  // the misaligned product gathers nothing without the transpose
+    set_error("vs_gather_floor of a misaligned direction needs vs_attach_transpose");
+    return VS_ERR_UNSUPPORTED;
+  }
+  const Matrix &m = aligned ? A->A : *A->T;
+  if (w == 0 || m.nnz == 0) return VS_OK;
+  if (rows > 0 && !X.p) return invalid("B pointer is NULL");
+  int n_sm = 0, dev = 0;
+  VS_CUDA(cudaGetDevice(&dev));
+  VS_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+  const unsigned grid = (unsigned)(n_sm * 8);
+  VS_TRY(A->floor_sink.reserve(sizeof(float) * grid * 256, stream));
+  vs_derive::gather_floor_kernel<8><<<grid, 256, 0, stream>>>(
+      m.idx, m.nnz, static_cast<const float4 *>(X.p), X.ld / 4, (int)(w / 4),
+      static_cast<float *>(A->floor_sink.p));
+  VS_LAUNCH_CHECK();
+  return VS_OK;
+}
+
 vs_status vs_info(vs_handle A, vs_info_t *info) {
   if (!valid_handle(A) || !info) return invalid("NULL argument");
   const Matrix &m = A->A;
@@ -655,6 +739,10 @@ vs_status vs_destroy(vs_handle A) {
   A->tp_table.release();
   A->stage_B.release();
   A->stage_out.release();
+  A->view_vals.release();
+  A->view_tvals.release();
+  A->view_X.release();
+  A->floor_sink.release();
   delete A;
   return VS_OK;
 }

@@ -127,6 +127,7 @@ struct vs_handle_s {
   vs::Scratch tp_table;      // two-phase tile offsets
   vs::Scratch stage_B, stage_out;  // host-operand staging (vs_spmm_host)
   vs::Scratch view_vals, view_tvals, view_X;  // normalized views: mapped values, scaled X
+  vs::Scratch floor_sink;                      // vs_gather_floor's per-thread sums
 };
 
 namespace vs {
