@@ -337,6 +337,24 @@ int32_t vs_version(void);
 int64_t vs_kernel_launches(void);
 
 /*
+ * vs_device_status -- synchronises `stream` and reports whether a product
+ * kernel on A gave up a bounded wait (every mbarrier wait of the kernels ends
+ * after about a second; the kernel then marks the handle, lets its own copies
+ * land and exits, leaving its output invalid and the context usable).
+ * Returns VS_ERR_TIMEOUT once per such event (the mark is cleared), else
+ * VS_OK.  vs_spmm_host calls it before returning.
+ */
+vs_status vs_device_status(vs_handle A, cudaStream_t stream);
+
+/*
+ * vs_test_stall_producers -- test hook for the failure path above: the next
+ * `launches` gather launches (process-wide) run with a producer that issues
+ * nothing, so their consumers' waits run out and the handle is marked.
+ * Nothing faults or hangs; each such launch takes about a second.  0 cancels.
+ */
+void vs_test_stall_producers(int launches);
+
+/*
  * vs_gather_floor -- a measurement, not a product: the memory-side floor of
  * the gather that vs_spmm(A, B, dir, VS_DETERMINISTIC) runs.  One kernel
  * reads every stored index of the matrix that product walks (the attached

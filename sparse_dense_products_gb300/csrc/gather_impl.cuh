@@ -56,6 +56,7 @@ struct GatherArgs {
   int n_x;         // rows of X (shared-memory variant: rows copied into the slab)
   void *partials;  // [n_shares][kMaxBlockWidth] of T
   const void *yscale;  // optional: Y[s, :] *= yscale[s] at the store
+  int stall;           // test hook: the producer issues nothing (see vs_test_stall_producers)
 };
 
 // Where the rows X[t, :] come from.  Each lane holds the address of its own
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
   grid_dependency_wait();  // may start while the previous kernel of the stream finishes
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (wid >= NW) {  // the producer warp(s)
+    if (a.stall) return;  // nothing issued: every consumer wait gives up after its limit
     if constexpr (Shape::kExpanders == 0)
       pipe.produce(a.st, blockIdx.x, a.st.n_blocks, gridDim.x);
     else if (wid == NW)
@@ -492,6 +494,7 @@ vs_status launch_typed(const Matrix &m, DenseView X, DenseView Y, int64_t w, cud
     a.n_x = (int)m.n_minor;
     a.partials = m.partials;
     a.yscale = Y.scale;
+    a.stall = take_stall() ? 1 : 0;
     int per_sm = 0;
     VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(k), Shape::kThreads, smem, &per_sm));
     const int64_t grid = std::min<int64_t>(m.n_blocks, (int64_t)std::max(1, per_sm) * m.n_sm);

@@ -97,6 +97,17 @@ void free_matrix(Matrix &m) {
   m.err = nullptr;
 }
 
+namespace {
+std::atomic<int> g_stall_launches{0};
+}  // namespace
+
+bool take_stall() {
+  int n = g_stall_launches.load();
+  while (n > 0 && !g_stall_launches.compare_exchange_weak(n, n - 1)) {
+  }
+  return n > 0;
+}
+
 vs_status kernel_occupancy(const void *kernel, int threads, int smem, int *per_sm) {
   static std::mutex mu;
   static std::map<std::tuple<int, const void *, int, int>, int> cache;
@@ -527,8 +538,7 @@ vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_
   else
     VS_CUDA(cudaMemcpy2DAsync(Y.p, Y.ld * es, A->stage_out.p, wpad * es, w * es, Y.rows,
                               cudaMemcpyDeviceToHost, stream));
-  VS_CUDA(cudaStreamSynchronize(stream));
-  return VS_OK;
+  return vs_device_status(A, stream);  // synchronises; reports a gave-up wait
 }
 
 vs_status vs_attach_transpose(vs_handle A, cudaStream_t stream) {
@@ -681,6 +691,26 @@ vs_status vs_gather_floor(vs_handle A, const vs_dense *B, vs_direction dir, cuda
   VS_LAUNCH_CHECK();
   return VS_OK;
 }
+
+vs_status vs_device_status(vs_handle A, cudaStream_t stream) {
+  if (!valid_handle(A)) return invalid("NULL handle");
+  VS_CUDA(cudaStreamSynchronize(stream));
+  int flags = 0;
+  for (Matrix *m : {&A->A, A->T}) {
+    if (!m || !m->err) continue;
+    int f = 0;
+    VS_CUDA(cudaMemcpy(&f, m->err, sizeof f, cudaMemcpyDeviceToHost));
+    if (f) VS_CUDA(cudaMemset(m->err, 0, sizeof f));
+    flags |= f;
+  }
+  if (flags) {
+    set_error("a product kernel's bounded wait gave up; its output is not valid");
+    return VS_ERR_TIMEOUT;
+  }
+  return VS_OK;
+}
+
+void vs_test_stall_producers(int launches) { g_stall_launches.store(launches < 0 ? 0 : launches); }
 
 vs_status vs_info(vs_handle A, vs_info_t *info) {
   if (!valid_handle(A) || !info) return invalid("NULL argument");

@@ -186,6 +186,11 @@ vs_status launch_scatter_two_phase_static(const Matrix &m, DenseView X, DenseVie
 // a product's host path makes no such query after its first call.
 vs_status kernel_occupancy(const void *kernel, int threads, int smem, int *per_sm);
 
+// Test hook of the failure path (vs_test_stall_producers): true when this
+// gather launch's producer is to issue nothing, so that its consumers' bounded
+// waits run out.
+bool take_stall();
+
 // Y[0:rows, 0:w] = 0 with row stride ld.
 vs_status launch_zero_fill(DenseView Y, int64_t w, size_t dsize, cudaStream_t s);
 
