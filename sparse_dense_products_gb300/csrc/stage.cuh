@@ -8,15 +8,17 @@
 //   * a chunk block: chunk k, entries [e0, e1), of a long slice s0; the chunk
 //     is further cut into shares of kShareEntries entries.
 //
-// Each CTA runs a producer/consumer pipeline over its blocks.  One producer
-// warp brings a block's index, value, slice-pointer and run arrays into one of
-// kStages shared-memory buffers with bulk copies (cp.async.bulk), signalled on
-// the buffer's "full" mbarrier; the consumer warps (kWarpsPerCta, or the
-// count the kernel passes to Pipe::init) take work
-// units of the block (groups of slices, or shares) from a per-buffer counter
-// and, when the block has no work left, arrive on its "empty" mbarrier, which
-// lets the producer refill the buffer.  Warps never wait for one another
-// except through these barriers, and every wait is bounded in time.
+// Each CTA runs a producer/consumer pipeline over its blocks.  A producer warp
+// brings a block's index, value, slice-pointer and run arrays, and its
+// descriptor, into one of the stage buffers with bulk copies (cp.async.bulk),
+// signalled on the buffer's "full" mbarrier.  For VCS the run values are then
+// expanded to one value per entry in shared memory (by the same warp, or by
+// dedicated expanding warps) and the buffer's "ready" mbarrier is signalled.
+// The consumer warps (kWarpsPerCta, or the count the kernel passes to
+// Pipe::init) take the block's work units (groups of slices, or shares) in a
+// round-robin the kernel fixes, and when done arrive on the buffer's "empty"
+// mbarrier, which lets the producer refill it.  Warps never wait for one
+// another except through these barriers, and every wait is bounded in time.
 #pragma once
 
 #include "device_utils.cuh"
@@ -71,7 +73,7 @@ struct StageLayout {
 };
 
 // Shared memory of a pipelined kernel with NS stage buffers: the buffers,
-// then the control words (full and empty barriers, work counters, failure
+// then the control words (full, empty and ready barriers, failure
 // flag), then `extra`.
 template <typename T, bool VCS, int NS = kStages>
 struct PipeLayout {
@@ -79,8 +81,7 @@ struct PipeLayout {
   static constexpr int kFull = NS * StageLayout<T, VCS>::kBytes;
   static constexpr int kEmpty = kFull + 8 * NS;
   static constexpr int kReady = kEmpty + 8 * NS;  // VCS: run values expanded
-  static constexpr int kCounter = kReady + 8 * NS;
-  static constexpr int kFail = kCounter + 4 * NS;
+  static constexpr int kFail = kReady + 8 * NS;
   static constexpr int kExtra = (kFail + 4 + 127) / 128 * 128;
 };
 
@@ -270,9 +271,6 @@ struct Pipe {
   __device__ __forceinline__ uint64_t *ready(int s) const {
     return reinterpret_cast<uint64_t *>(smem + PL::kReady) + s;
   }
-  __device__ __forceinline__ int *counter(int s) const {
-    return reinterpret_cast<int *>(smem + PL::kCounter) + s;
-  }
   __device__ __forceinline__ int *fail() const { return reinterpret_cast<int *>(smem + PL::kFail); }
 
   // All threads; contains __syncthreads.  `consumers`: warps that release
@@ -380,7 +378,6 @@ struct Pipe {
       int4 d[3];
       win.get(a.blocks, b_begin, step, b_end, i, d);
       if (lane == 0) {
-        *counter(i % NS) = 0;
         stage_issue<T, VCS>(a, d, buf(i % NS), full(i % NS));
       }
       __syncwarp();
@@ -461,7 +458,6 @@ struct Pipe {
       int4 d[3];
       win.get(a.blocks, b_begin, step, b_end, issued, d);
       if (lane == 0) {
-        *counter(s) = 0;
         stage_issue<T, VCS>(a, d, buf(s), full(s));
       }
       __syncwarp();
@@ -500,13 +496,6 @@ struct Pipe {
   __device__ __forceinline__ void release(int i) const {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(empty(i % NS));
-  }
-
-  // Consumer warp: next work unit of the i-th block (warp-uniform).
-  __device__ __forceinline__ int grab(int i) const {
-    int u = 0;
-    if ((threadIdx.x & 31) == 0) u = atomicAdd(counter(i % NS), 1);
-    return __shfl_sync(kFullMask, u, 0);
   }
 };
 
