@@ -239,10 +239,15 @@ def reference_arm(args):
     from sparse_dense_products_gb300 import workloads as W
     import oracle
 
+    import torch
+
     oracle.build()
-    coo = W.make(WORKLOAD, seed=0)
-    Bab = W.dense(coo.n_cols, WIDTH, seed=1).double().numpy()
-    Bba_rows = W.dense(coo.n_rows, WIDTH, seed=2).double().numpy()
+    # the same matrix and operands as the GPU arm (the generators' draws differ
+    # between devices, so generate where that arm does when a GPU is present)
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    coo = W.make(WORKLOAD, seed=0, device=gen).to("cpu")
+    Bab = W.dense(coo.n_cols, WIDTH, seed=1, device=gen).double().cpu().numpy()
+    Bba_rows = W.dense(coo.n_rows, WIDTH, seed=2, device=gen).double().cpu().numpy()
     per = layout_bytes_host(coo)
     total_bytes = sum(per)
     trip = oracle_prepare(coo)
@@ -260,8 +265,9 @@ def reference_arm(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / reps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "main: 60000x2000 count matrix, 6.02M nnz, width 16, six products",
-                   "l2": "n/a (host)"},
+        "config": {"workload": "main: 60000x2000 count matrix, %d nnz, width 16, six products "
+                               "(VCSR@B VCSC@B B@VCSR B@VCSC CSR@B B@CSR), float64 oracle" % coo.nnz,
+                   "l2": "n/a (host)", "generated_on": gen},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": "full workload, six float64 oracle products per step"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
