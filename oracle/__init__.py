@@ -55,31 +55,54 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _configure(lib):
+    """Declares the C signatures on a loaded oracle library."""
+    i64, i32p, vp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
+    lib.or_csr_build.restype = ctypes.c_int
+    lib.or_csr_build.argtypes = [i64, i64, i64, i32p, i32p, vp, i64, i32p, i32p, vp]
+    lib.or_vcs_build.restype = ctypes.c_int64
+    lib.or_vcs_build.argtypes = [i64, i64, i64, i32p, i32p, vp, i32p, vp, i32p, i32p]
+    lib.or_csr_triples.restype = None
+    lib.or_csr_triples.argtypes = [i64, ctypes.c_int, i32p, i32p, vp, i32p, i32p, vp]
+    lib.or_vcs_triples.restype = None
+    lib.or_vcs_triples.argtypes = [i64, ctypes.c_int, i32p, vp, i32p, i32p, i32p, i32p, vp]
+    for name in ("or_spmm_ab", "or_spmm_ba"):
+        f = getattr(lib, name)
+        f.restype = None
+        f.argtypes = [i64, i64, i64, i32p, i32p, vp, vp, i64, i64, vp, vp, i64]
+    for name in ("or_spmm_ab_rows", "or_spmm_ba_cols"):
+        f = getattr(lib, name)
+        f.restype = None
+        f.argtypes = [i64, i64, i32p, i32p, vp, vp, i64, i64, i64, vp, vp, vp, vp]
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
-        i64, i32p, vp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
-        lib.or_csr_build.restype = ctypes.c_int
-        lib.or_csr_build.argtypes = [i64, i64, i64, i32p, i32p, vp, i64, i32p, i32p, vp]
-        lib.or_vcs_build.restype = ctypes.c_int64
-        lib.or_vcs_build.argtypes = [i64, i64, i64, i32p, i32p, vp, i32p, vp, i32p, i32p]
-        lib.or_csr_triples.restype = None
-        lib.or_csr_triples.argtypes = [i64, ctypes.c_int, i32p, i32p, vp, i32p, i32p, vp]
-        lib.or_vcs_triples.restype = None
-        lib.or_vcs_triples.argtypes = [i64, ctypes.c_int, i32p, vp, i32p, i32p, i32p, i32p, vp]
-        for name in ("or_spmm_ab", "or_spmm_ba"):
-            f = getattr(lib, name)
-            f.restype = None
-            f.argtypes = [i64, i64, i64, i32p, i32p, vp, vp, i64, i64, vp, vp, i64]
-        for name in ("or_spmm_ab_rows", "or_spmm_ba_cols"):
-            f = getattr(lib, name)
-            f.restype = None
-            f.argtypes = [i64, i64, i32p, i32p, vp, vp, i64, i64, i64, vp, vp, vp, vp]
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = _configure(ctypes.CDLL(build()))
+        return _lib
+
+
+class use_library:
+    """Test hook: run the oracle functions on another build of vs_oracle.c (a
+    copy with a planted mistake, to check that the pins catch it)."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        with _lock:
+            self.saved = _lib
+            _lib = _configure(ctypes.CDLL(self.path))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self.saved
 
 
 def _p(a: np.ndarray):
