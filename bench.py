@@ -12,9 +12,12 @@ reported beside them.
 
 Metric: effective HBM GB/s = algorithmic bytes / device time, where the
 algorithmic bytes of a product are every array of the stored layout, the dense
-operand read once and the output written once.  L2 is flushed (a 512 MiB
-write) before every timed product; CUDA events bracket each product on the
-launching stream; a product's time is the median over the timed steps.
+operand read once and the output written once.  L2 is flushed before every
+timed product: a 512 MiB buffer is written and then read back, so that L2 holds
+only clean lines of that buffer (none of the product's data, and no dirty
+lines whose write-back the product would otherwise pay for).  CUDA events
+bracket each product on the launching stream; a product's time is the median
+over the timed steps.
 
 ``--impl reference`` times the float64 CPU oracle on the same workload and
 metric (the deliberately slow reference; host cores).
@@ -344,13 +347,21 @@ def gpu_arm(args):
               for name, layout, major, direction in PRODUCTS}
 
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush_sum = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        """Write a buffer four times the size of L2, then read it back: the
+        read evicts the dirty lines the write left, so L2 ends holding clean
+        lines of this buffer only."""
+        flush.fill_(1.0)
+        torch.sum(flush, dtype=torch.float32, out=flush_sum)
     stream = torch.cuda.current_stream(dev)
 
     def timed(fn, reps):
         """Device ms of fn() per rep, L2 flushed before each rep (events after the flush)."""
         evs = []
         for _ in range(reps):
-            flush.fill_(1.0)
+            flush_l2()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -478,7 +489,7 @@ def gpu_arm(args):
     for it in range(args.warmup + args.steps):
         tot = 0.0
         for name, layout, major, direction in PRODUCTS:
-            flush.fill_(1.0)
+            flush_l2()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             vs.spmm_host(handles[(layout, major)], Bab_h if direction == "A@B" else Bt_h.t(),
@@ -533,7 +544,7 @@ def gpu_arm(args):
         "config": {"workload": "main: 60000x2000 count matrix, %d nnz, width 16, six products "
                                "(VCSR@B VCSC@B B@VCSR B@VCSC CSR@B B@CSR), deterministic; "
                                "misaligned ones over the attached exact transpose" % coo.nnz,
-                   "l2": "flushed before every product (512 MiB write)",
+                   "l2": "flushed before every product (512 MiB written, then read back)",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "ms_per_product": round(t_max / len(PRODUCTS), 5),
         "frac_of_8TBs": round(value / ws / NOMINAL_HBM_GBS, 4),
