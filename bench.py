@@ -354,7 +354,7 @@ def gpu_arm(args):
         read evicts the dirty lines the write left, so L2 ends holding clean
         lines of this buffer only."""
         flush.fill_(1.0)
-        torch.sum(flush, dtype=torch.float32, out=flush_sum)
+        flush_sum.copy_(flush.sum())
     stream = torch.cuda.current_stream(dev)
 
     def timed(fn, reps):
