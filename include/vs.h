@@ -256,9 +256,19 @@ vs_status vs_spmm_view(vs_handle A, const vs_dense *B, const vs_dense *out, vs_d
 /*
  * vs_spmm_host -- vs_spmm with B and out in HOST memory (pinned memory is
  * fastest).  Copies B to device staging owned by the handle, runs vs_spmm on
- * `stream`, copies the result back and synchronises `stream` before
+ * `stream`, copies the result back and synchronises `stream` once before
  * returning, so `out` is ready on return.  Layout rules as for vs_spmm.  The
- * staging buffers grow on first use with a larger operand.
+ * staging buffers grow on first use with a larger operand; a pinned 8-byte
+ * status area is allocated on the first call and freed by vs_destroy.
+ * A pinned, device-mapped B is staged by a copy kernel reading it through
+ * its mapping (loads from every multiprocessor), any other B by the copy
+ * engine.  When `out` is pinned host memory mapped into the device's address space
+ * (cudaHostAlloc, cudaHostRegister, torch pin_memory) and the product runs as
+ * a gather (an aligned product, or VS_DETERMINISTIC / VS_TRANSPOSED over an
+ * attached transpose), the kernels store the result straight into it and no
+ * copy back is made; elements outside the logical output are never written.
+ * Errors: as vs_spmm; VS_ERR_TIMEOUT (and the mark cleared, as by
+ * vs_device_status) when a product kernel's bounded wait gave up.
  */
 vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_host,
                        vs_direction dir, vs_variant variant, cudaStream_t stream);

@@ -270,6 +270,23 @@ vs_status frame(const Matrix &m, const vs_dense &B, const vs_dense &out, vs_dire
 }  // namespace
 
 namespace vs_derive {
+// Copies `rows` rows of `row_bytes` bytes from host memory mapped into the
+// device's address space (src, pitch src_ld bytes) to device memory (dst,
+// pitch dst_ld bytes), U bytes per load: many SMs' loads in flight over the
+// CPU-GPU link.  U divides row_bytes and both pitches; both bases are U-aligned.
+template <typename U>
+__global__ void copy_rows_kernel(const char *__restrict__ src, int64_t src_ld, char *__restrict__ dst,
+                                 int64_t dst_ld, int64_t rows, int64_t row_bytes) {
+  const int64_t per_row = row_bytes / (int64_t)sizeof(U);
+  const int64_t total = rows * per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / per_row, c = i - r * per_row;
+    *reinterpret_cast<U *>(dst + r * dst_ld + c * (int64_t)sizeof(U)) =
+        *reinterpret_cast<const U *>(src + r * src_ld + c * (int64_t)sizeof(U));
+  }
+}
+
 // values[e] * factors[e], one rounding in T (vs_scale_entries)
 template <typename T>
 __global__ void scale_values_kernel(const T *__restrict__ v, const T *__restrict__ f, int64_t n,
@@ -514,10 +531,47 @@ vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_
   if (w == 0 || Y.rows == 0) return VS_OK;
   const size_t es = X.f64 ? 8 : 4;
   const int64_t wpad = (w + 3) / 4 * 4;  // keep device rows 16-byte aligned
+  // Gather routes store every output element exactly once with plain stores,
+  // so a pinned, device-mapped `out` is written in place by the kernel (over
+  // the CPU-GPU link, while it computes) instead of staged and copied back.
+  const bool gather_route =
+      aligned || variant == VS_TRANSPOSED || (variant == VS_DETERMINISTIC && A->T);
+  void *out_dev = nullptr;
+  if (gather_route) {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, out_host->ptr) == cudaSuccess &&
+        pa.type == cudaMemoryTypeHost && pa.devicePointer)
+      out_dev = pa.devicePointer;
+    else
+      cudaGetLastError();  // not mapped: staged below
+  }
   VS_TRY(A->stage_B.reserve((size_t)std::max<int64_t>(X.rows, 1) * wpad * es, stream));
-  VS_TRY(A->stage_out.reserve((size_t)Y.rows * wpad * es, stream));
-  // one linear copy when the host rows are already at the device pitch
-  if (X.rows > 0 && X.ld == wpad && w == wpad)
+  if (!out_dev) VS_TRY(A->stage_out.reserve((size_t)Y.rows * wpad * es, stream));
+  // B from mapped (pinned) host memory: a copy kernel, whose loads from every
+  // SM keep more of the CPU-GPU link busy than one copy engine does
+  void *b_dev = nullptr;
+  if (X.rows > 0) {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, B_host->ptr) == cudaSuccess &&
+        pa.type == cudaMemoryTypeHost && pa.devicePointer)
+      b_dev = pa.devicePointer;
+    else
+      cudaGetLastError();  // not mapped: copied by the copy engine below
+  }
+  if (b_dev) {
+    const int64_t rb = w * (int64_t)es, sld = X.ld * (int64_t)es, dld = wpad * (int64_t)es;
+    const bool v16 = rb % 16 == 0 && sld % 16 == 0 && reinterpret_cast<uintptr_t>(b_dev) % 16 == 0;
+    const int64_t units = X.rows * (rb / (v16 ? 16 : 4));
+    const unsigned grid =
+        (unsigned)std::max<int64_t>(1, std::min<int64_t>((int64_t)A->A.n_sm * 8, (units + 255) / 256));
+    if (v16)
+      vs_derive::copy_rows_kernel<uint4><<<grid, 256, 0, stream>>>(
+          static_cast<const char *>(b_dev), sld, static_cast<char *>(A->stage_B.p), dld, X.rows, rb);
+    else
+      vs_derive::copy_rows_kernel<uint32_t><<<grid, 256, 0, stream>>>(
+          static_cast<const char *>(b_dev), sld, static_cast<char *>(A->stage_B.p), dld, X.rows, rb);
+    VS_LAUNCH_CHECK();
+  } else if (X.rows > 0 && X.ld == wpad && w == wpad)
     VS_CUDA(cudaMemcpyAsync(A->stage_B.p, X.p, (size_t)X.rows * wpad * es,
                             cudaMemcpyHostToDevice, stream));
   else if (X.rows > 0)
@@ -531,14 +585,36 @@ vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_
     Bd = vs_dense{A->stage_B.p, B_host->rows, B_host->cols, 1, wpad, B_host->dtype};
     Od = vs_dense{A->stage_out.p, out_host->rows, out_host->cols, 1, wpad, out_host->dtype};
   }
+  if (out_dev) {
+    Od = *out_host;
+    Od.ptr = out_dev;
+  }
   VS_TRY(vs_spmm(A, &Bd, &Od, dir, variant, stream));
-  if (Y.ld == wpad && w == wpad)
+  if (out_dev) {
+    // written in place
+  } else if (Y.ld == wpad && w == wpad)
     VS_CUDA(cudaMemcpyAsync(Y.p, A->stage_out.p, (size_t)Y.rows * wpad * es,
                             cudaMemcpyDeviceToHost, stream));
   else
     VS_CUDA(cudaMemcpy2DAsync(Y.p, Y.ld * es, A->stage_out.p, wpad * es, w * es, Y.rows,
                               cudaMemcpyDeviceToHost, stream));
-  return vs_device_status(A, stream);  // synchronises; reports a gave-up wait
+  // the failure flags come back with the output, so one synchronisation ends the call
+  if (!A->host_flags) {
+    void *hf = nullptr;
+    VS_CUDA(cudaHostAlloc(&hf, 2 * sizeof(int), cudaHostAllocDefault));
+    A->host_flags = static_cast<int *>(hf);
+  }
+  const Matrix *ms[2] = {&A->A, A->T};
+  for (int k = 0; k < 2; ++k) {
+    A->host_flags[k] = 0;
+    if (ms[k] && ms[k]->err)
+      VS_CUDA(cudaMemcpyAsync(A->host_flags + k, ms[k]->err, sizeof(int), cudaMemcpyDeviceToHost,
+                              stream));
+  }
+  VS_CUDA(cudaStreamSynchronize(stream));
+  if (A->host_flags[0] | A->host_flags[1])
+    return vs_device_status(A, stream);  // clears the flags; reports the gave-up wait
+  return VS_OK;
 }
 
 vs_status vs_attach_transpose(vs_handle A, cudaStream_t stream) {
@@ -749,7 +825,7 @@ vs_status vs_handle_bytes(vs_handle A, int64_t *layout_bytes, int64_t *scratch_b
   if (!valid_handle(A)) return invalid("NULL handle");
   if (layout_bytes) *layout_bytes = A->A.layout_bytes();
   if (scratch_bytes) {
-    int64_t s = A->A.meta_bytes() + (int64_t)A->tp_partials.bytes + (int64_t)A->tp_table.bytes +
+    int64_t s = A->A.meta_bytes() + (int64_t)A->tp_partials.bytes +
                 (int64_t)A->stage_B.bytes + (int64_t)A->stage_out.bytes;
     if (A->T) s += A->T->layout_bytes() + A->T->meta_bytes();
     *scratch_bytes = s;
@@ -766,7 +842,7 @@ vs_status vs_destroy(vs_handle A) {
     delete A->T;
   }
   A->tp_partials.release();
-  A->tp_table.release();
+  if (A->host_flags) cudaFreeHost(A->host_flags);
   A->stage_B.release();
   A->stage_out.release();
   A->view_vals.release();

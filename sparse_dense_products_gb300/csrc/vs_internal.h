@@ -124,8 +124,8 @@ struct vs_handle_s {
   vs::Matrix *T = nullptr;  // exact transpose (other major), once attached
   int device = 0;
   vs::Scratch tp_partials;   // two-phase chunk partials
-  vs::Scratch tp_table;      // two-phase tile offsets
   vs::Scratch stage_B, stage_out;  // host-operand staging (vs_spmm_host)
+  int *host_flags = nullptr;       // pinned: the failure flags of A and T, read back by vs_spmm_host
   vs::Scratch view_vals, view_tvals, view_X;  // normalized views: mapped values, scaled X
   vs::Scratch floor_sink;                      // vs_gather_floor's per-thread sums
 };

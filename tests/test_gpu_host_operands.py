@@ -1,7 +1,8 @@
 """vs_spmm_host: the product with B and out in host memory (the end-to-end
 path of the benchmark) equals the device product bit for bit, for pinned and
-pageable buffers, pitched and strided host views, and leaves host memory
-outside the logical output untouched."""
+pageable buffers (a pinned output of a gather is written in place by the
+kernel, a pageable one is staged and copied back), pitched and strided host
+views, and leaves host memory outside the logical output untouched."""
 import pytest
 import torch
 
@@ -24,9 +25,9 @@ def _host_out(A, w, direction, dtype, pin, pad):
     """A host output of the product's shape inside a wider (or taller) NaN-filled buffer."""
     n_rows, n_cols = A.shape
     if direction == "A@B":
-        big = torch.full((n_rows, w + pad), float("nan"), dtype=dtype)
+        big = torch.full((n_rows, w + pad), float("nan"), dtype=dtype, pin_memory=pin)
         return big, big[:, :w]
-    big = torch.full((w + pad, n_cols), float("nan"), dtype=dtype).t().contiguous().t()
+    big = torch.full((n_cols, w + pad), float("nan"), dtype=dtype, pin_memory=pin).t()
     return big, big[:w, :]
 
 
@@ -38,11 +39,14 @@ def test_host_operands_match_device_product(layout, major, direction, w, pad, pi
     A.attach_transpose()
     B, _ = dense_operand(coo, direction, w, torch.float32, seed=3)
     want = vs.spmm(A, B, direction).cpu()
-    Bh = B.cpu()
-    if pin:
-        Bh = Bh.pin_memory()
-    if direction == "B@A":           # the host operand keeps the width-contiguous layout
-        Bh = Bh.t().contiguous().t()
+    if direction == "A@B":
+        Bh = B.cpu()
+        if pin:                      # pinned: read by a copy kernel through its mapping
+            Bh = Bh.pin_memory()
+    else:                            # the host operand keeps the width-contiguous layout
+        Bh = torch.empty(B.shape[1], B.shape[0], dtype=B.dtype, pin_memory=pin)
+        Bh.copy_(B.t().cpu())
+        Bh = Bh.t()
     big, out = _host_out(A, w, direction, torch.float32, pin, pad)
     vs.spmm_host(A, Bh, direction, "deterministic", out=out)
     assert torch.equal(out, want)
@@ -59,4 +63,23 @@ def test_host_operands_mixed_precision():
     want = vs.spmm(A, B, "A@B").cpu()
     got = vs.spmm_host(A, B.cpu().pin_memory(), "A@B", "deterministic")
     assert got.dtype == torch.float64 and torch.equal(got, want)
+    A.destroy()
+
+
+@pytest.mark.parametrize("variant", ["two_phase", "transposed"])
+def test_host_operands_misaligned_variants(variant):
+    # two_phase stages the output and copies it back; transposed (a gather)
+    # writes the pinned output in place: both equal the device product
+    coo = W.random_coo(700, 500, 30_000, seed=63, values="counts", sort=False)
+    A = build(coo, "vcs", "row")
+    A.attach_transpose()
+    B, _ = dense_operand(coo, "B@A", 16, torch.float32, seed=5)
+    want = vs.spmm(A, B, "B@A", variant).cpu()
+    Bh = B.cpu().t().contiguous().t()            # width-contiguous, pageable
+    # a pinned, width-contiguous output inside a taller NaN-filled buffer
+    big = torch.empty(coo.n_cols, 16 + 2, pin_memory=True).fill_(float("nan")).t()
+    out = big[:16, :]
+    vs.spmm_host(A, Bh, "B@A", variant, out=out)
+    assert torch.equal(out, want)
+    assert torch.isnan(big[16:, :]).all(), "host memory outside the output was written"
     A.destroy()
