@@ -211,6 +211,24 @@ struct TwoPhaseSmem {
   static constexpr int kTile = kPrep + kPreparers * PrepLayout::kBytes;
 };
 
+// First position p in [lo, hi) with idx[p] >= key (hi if none) over indices
+// that ascend on [lo, hi), by the whole warp: while more than 32 candidates
+// remain, the lanes test the starts of 32 equal segments and the ballot
+// keeps the segment holding the boundary; then each lane tests one candidate.
+// A block's run (at most kBlockEntries entries) takes two rounds of loads.
+__device__ __forceinline__ int warp_lower_bound(const int32_t *idx, int lo, int hi, int key) {
+  const int lane = threadIdx.x & 31;
+  while (hi - lo > 32) {
+    const int step = (hi - lo + 31) / 32;
+    const int p = lo + (lane + 1) * step;
+    const int nl = __popc(__ballot_sync(kFullMask, p < hi && idx[p] < key));
+    lo += nl * step;
+    hi = min(lo + step, hi);
+  }
+  const int p = lo + lane;
+  return lo + __popc(__ballot_sync(kFullMask, p < hi && idx[p] < key));
+}
+
 // Producer warp: once block j (number b) has landed, write the records of its
 // entries that fall in rows [t0, t0 + rows), in entry order, and mark the
 // stage ready.  The slice of an entry and (VCS) its run come from start
@@ -339,20 +357,8 @@ __device__ __forceinline__ bool two_phase_prepare(const Pipe<T, VCS> &pipe, cons
         if (pass == 0) {
           const int lo = max(sv.vptr[r], k.e0), hi = min(sv.vptr[r + 1], k.e1);
           // first entry with row >= t0, then first with row >= t0 + rows
-          int x0 = lo, x1 = hi;
-          while (x0 < x1) {
-            const int mid = (x0 + x1) >> 1;
-            if (sv.idx[mid] < t0) x0 = mid + 1;
-            else x1 = mid;
-          }
-          int y0 = x0, y1 = hi;
-          while (y0 < y1) {
-            const int mid = (y0 + y1) >> 1;
-            if (sv.idx[mid] < t0 + rows) y0 = mid + 1;
-            else y1 = mid;
-          }
-          a0 = x0;
-          b0 = y0;
+          a0 = warp_lower_bound(sv.idx, lo, hi, (int)t0);
+          b0 = warp_lower_bound(sv.idx, a0, hi, (int)(t0 + rows));
           if (lane == 0) {
             rng[2 * (r - k.r0)] = a0;
             rng[2 * (r - k.r0) + 1] = b0;
