@@ -67,6 +67,9 @@ class VsError(RuntimeError):
 def load() -> ctypes.CDLL:
     """Loads libvs.so (raises if it has not been built)."""
     global _lib
+    lib = _lib
+    if lib is not None:  # loaded: no lock on the per-call path
+        return lib
     with _lock:
         if _lib is not None:
             return _lib

@@ -194,10 +194,12 @@ def build_vcs(rows: torch.Tensor, cols: torch.Tensor, vals: torch.Tensor, shape,
 def _dense(t: torch.Tensor) -> L.Dense:
     if t.dim() != 2:
         raise ValueError("dense operands are 2-D")
-    if t.dtype not in _DTYPES:
+    dt = _DTYPES.get(t.dtype)
+    if dt is None:
         raise TypeError("dense operands must be float32 or float64")
-    return L.Dense(t.data_ptr() if t.numel() else 0, t.shape[0], t.shape[1], t.stride(0),
-                   t.stride(1), _DTYPES[t.dtype])
+    rows, cols = t.shape
+    rs, cs = t.stride()
+    return L.Dense(t.data_ptr() if rows and cols else 0, rows, cols, rs, cs, dt)
 
 
 def empty_out(A: SparseMatrix, w: int, direction: str = "A@B", dtype=None, device=None,
