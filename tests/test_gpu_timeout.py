@@ -48,3 +48,22 @@ def test_stalled_producer_times_out_and_the_handle_recovers(layout, n_cols):
     assert_close(got, want, D, TOL[torch.float32], "after the timeout")
     assert _status(A) == "VS_OK"
     A.destroy()
+
+
+def test_host_entry_reports_the_timeout_and_recovers():
+    # vs_spmm_host reads the handle's marks back with its output: a stalled
+    # gather comes back as VS_ERR_TIMEOUT from the call itself, once
+    coo = W.random_coo(2000, 700, 50_000, seed=82, values="counts", sort=False)
+    A = build(coo, "vcs", "row")
+    B, Bt = dense_operand(coo, "A@B", 16, torch.float32)
+    Bh = B.cpu().pin_memory()
+    out = vs.empty_out(A, 16, "A@B", device="cpu", pin_memory=True)
+    L.load().vs_test_stall_producers(1)
+    with pytest.raises(L.VsError) as e:
+        vs.spmm_host(A, Bh, "A@B", "deterministic", out=out)
+    assert L.STATUS[e.value.status] == "VS_ERR_TIMEOUT"
+    assert _status(A) == "VS_OK"                      # reported once
+    vs.spmm_host(A, Bh, "A@B", "deterministic", out=out)
+    want, D = oracle_product(coo, oracle_triples(coo, "vcs", "row"), "A@B", Bt)
+    assert_close(out.double().numpy(), want, D, TOL[torch.float32], "after the timeout")
+    A.destroy()
