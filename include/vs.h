@@ -37,6 +37,11 @@
  *    row axis (B and out stored column-major).  Otherwise VS_ERR_LAYOUT.
  *  - out is overwritten (beta = 0).  A slice with no entries yields zeros.
  *    B and out must not overlap.
+ *  - A handle's scratch (long-slice share partials, two-phase partials,
+ *    host staging) serves every call on that handle: calls on one handle
+ *    from several host threads at once, or whose work overlaps on the GPU
+ *    (different streams), must be serialised by the caller.  Different
+ *    handles are independent.
  */
 #ifndef VS_H
 #define VS_H
