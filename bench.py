@@ -156,9 +156,10 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(product: str):
-    """DRAM bytes (read + write) of one launch of `product`'s kernel, from the ncu
-    record in profiles/dram_traffic.txt, or None when the kernels changed since."""
+def recorded_profile(key: str):
+    """A value recorded from ncu in profiles/dram_traffic.txt (a product's DRAM bytes
+    per launch, or "l1pct:<product>", its kernel's L1/shared throughput in % of peak),
+    or None when the record is missing or the CUDA sources changed since."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     try:
         rec = {}
@@ -169,9 +170,16 @@ def recorded_traffic(product: str):
                     rec[ln[0]] = ln[1]
         if rec.get("source_digest") != source_digest():
             return None
-        return int(rec[product])
+        return float(rec[key])
     except (OSError, KeyError, ValueError):
         return None
+
+
+def recorded_traffic(product: str):
+    """DRAM bytes (read + write) of one launch of `product`'s kernel, from the ncu
+    record in profiles/dram_traffic.txt, or None when the kernels changed since."""
+    v = recorded_profile(product)
+    return None if v is None else int(v)
 
 
 def algorithmic_bytes(A, n_x_rows: int, n_y_rows: int, w: int, es: int = 4) -> int:
@@ -523,7 +531,11 @@ def gpu_arm(args):
               "unit": "GB/s", "frac": round(onchip_ach / onchip_peak, 4),
               "bytes_per_launch": onchip_bytes,
               "gather_floor_ms": floor_ms[dom],
-              "product_over_floor": round(ms_prod[dom] / floor_ms[dom], 3)}
+              "product_over_floor": round(ms_prod[dom] / floor_ms[dom], 3),
+              # what ncu measured on the L1/shared data path of the same kernel (the
+              # nominal peak above counts 128 useful bytes per clock; random 64-byte
+              # rows cannot fill it), null once the kernels changed since the capture
+              "ncu_l1_shared_throughput_pct": recorded_profile("l1pct:" + dom)}
 
     # ---- CPU baseline: the float64 oracle on host cores (rank 0, N=1 only)
     cpu = None
