@@ -231,15 +231,34 @@ __global__ void __launch_bounds__(GatherShape<XS, VCS>::kThreads, GatherShape<XS
   // past w zero), while the producer already streams the first blocks
   T *slab = reinterpret_cast<T *>(smem + PipeLayout<TV, VCS, NS>::kExtra);
   if constexpr (XS) {
-    const int nv = a.n_x * Q;  // vectors per pass
-    for (int p = 0; p < npass; ++p)
-      for (int v = threadIdx.x; v < nv; v += NW * 32) {
-        const int r = v / Q, c = p * TW + (v % Q) * VEC;
-        V x{};
-        if (c < w) x = ld_gather(reinterpret_cast<const V *>(X + (int64_t)r * a.ldx + c));
-        *reinterpret_cast<V *>(slab + ((int64_t)p * a.n_x + r) * TW + (v % Q) * VEC) = x;
+    if (npass == 1 && w == TW && a.ldx == TW && (TW * sizeof(T)) % 16 == 0 &&
+        (reinterpret_cast<uintptr_t>(X) & 15) == 0) {
+      // X is already in the slab's layout (rows of exactly one pass): bulk
+      // copies bring it in while the producer streams the first blocks
+      const uint32_t total = (uint32_t)a.n_x * TW * (uint32_t)sizeof(T);
+      if (threadIdx.x == 0) {
+        constexpr uint32_t kChunk = 32768;
+        mbar_arrive_expect_tx(pipe.slab_landed(), total);
+        for (uint32_t off = 0; off < total; off += kChunk)
+          bulk_load(reinterpret_cast<unsigned char *>(slab) + off,
+                    reinterpret_cast<const unsigned char *>(X) + off, min(kChunk, total - off),
+                    pipe.slab_landed());
       }
-    named_barrier(1, NW * 32);
+      if (!mbar_wait_bounded(pipe.slab_landed(), 0, kWaitLimitNs)) {
+        pipe.give_up(a.st);
+        return;
+      }
+    } else {
+      const int nv = a.n_x * Q;  // vectors per pass
+      for (int p = 0; p < npass; ++p)
+        for (int v = threadIdx.x; v < nv; v += NW * 32) {
+          const int r = v / Q, c = p * TW + (v % Q) * VEC;
+          V x{};
+          if (c < w) x = ld_gather(reinterpret_cast<const V *>(X + (int64_t)r * a.ldx + c));
+          *reinterpret_cast<V *>(slab + ((int64_t)p * a.n_x + r) * TW + (v % Q) * VEC) = x;
+        }
+      named_barrier(1, NW * 32);
+    }
   }
   auto source = [&](int cp) {
     // this lane's columns in pass cp / TW; lanes past the width read column 0

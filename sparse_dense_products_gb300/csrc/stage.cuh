@@ -73,8 +73,8 @@ struct StageLayout {
 };
 
 // Shared memory of a pipelined kernel with NS stage buffers: the buffers,
-// then the control words (full, empty and ready barriers, failure
-// flag), then `extra`.
+// then the control words (full, empty and ready barriers, failure flag,
+// slab barrier), then `extra`.
 template <typename T, bool VCS, int NS = kStages>
 struct PipeLayout {
   static constexpr int kBufs = 0;
@@ -82,7 +82,8 @@ struct PipeLayout {
   static constexpr int kEmpty = kFull + 8 * NS;
   static constexpr int kReady = kEmpty + 8 * NS;  // VCS: run values expanded
   static constexpr int kFail = kReady + 8 * NS;
-  static constexpr int kExtra = (kFail + 4 + 127) / 128 * 128;
+  static constexpr int kSlab = kFail + 8;  // gather: the shared-memory copy of X landed
+  static constexpr int kExtra = (kSlab + 8 + 127) / 128 * 128;
 };
 
 template <typename T, bool VCS, int NS = kStages>
@@ -272,6 +273,9 @@ struct Pipe {
     return reinterpret_cast<uint64_t *>(smem + PL::kReady) + s;
   }
   __device__ __forceinline__ int *fail() const { return reinterpret_cast<int *>(smem + PL::kFail); }
+  __device__ __forceinline__ uint64_t *slab_landed() const {
+    return reinterpret_cast<uint64_t *>(smem + PL::kSlab);
+  }
 
   // All threads; contains __syncthreads.  `consumers`: warps that release
   // each buffer.
@@ -282,6 +286,7 @@ struct Pipe {
         mbar_init(empty(s), consumers);
         mbar_init(ready(s), 1);
       }
+      mbar_init(slab_landed(), 1);
       *fail() = 0;
       fence_barrier_init();
     }
