@@ -54,3 +54,20 @@ def test_library_is_built_for_sm_103a():
     flags = " ".join(vs_build.ARCH)
     assert "compute_103a" in flags and "sm_103a" in flags
     assert os.path.exists(vs_build.LIB)
+
+
+def test_dense_descriptors_marshal_shape_strides_and_dtype():
+    import torch
+
+    from sparse_dense_products_gb300 import api
+
+    t = torch.empty(60, 16, dtype=torch.float64).t()          # 16 x 60, width-contiguous
+    d = api._dense(t)
+    assert (d.rows, d.cols, d.row_stride, d.col_stride) == (16, 60, 1, 16)
+    assert d.ptr == t.data_ptr() and d.dtype == 1             # VS_F64
+    e = api._dense(torch.empty(0, 16))
+    assert not e.ptr and (e.rows, e.cols) == (0, 16)           # no storage: NULL pointer
+    with pytest.raises(ValueError):
+        api._dense(torch.empty(4))
+    with pytest.raises(TypeError):
+        api._dense(torch.empty(4, 4, dtype=torch.float16))
