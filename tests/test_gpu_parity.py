@@ -326,3 +326,24 @@ def test_regrid_workload(dtype, direction):
             if variant != "atomic":
                 for _ in range(3):
                     assert torch.equal(_run(A, B, direction, variant), out)
+
+
+@pytest.mark.parametrize("w", [16, 64])
+def test_two_phase_partial_tiles_sorted_runs_with_duplicates(w):
+    """VCSC@B and B@VCSR whose output spans several shared-memory tiles: the
+    two-phase records come from per-run searches and stay in entry order;
+    duplicate (row, column) entries land in the same step.  Against the oracle,
+    and bit-identical on repeats."""
+    coo = W.random_coo(6000, 4000, 200_000, seed=71, values="counts", duplicates=True,
+                       sort=False)
+    for major, direction in (("col", "A@B"), ("row", "B@A")):
+        A = build(coo, "vcs", major)
+        tri = oracle_triples(coo, "vcs", major)
+        B, Bt = dense_operand(coo, direction, w, torch.float32, seed=w)
+        want, D = oracle_product(coo, tri, direction, Bt)
+        out = vs.spmm(A, B, direction, "two_phase")
+        assert_close(gpu_out_rows(out, direction), want, D, TOL[torch.float32],
+                     f"two_phase vcs/{major} {direction} w={w}")
+        for _ in range(2):
+            assert torch.equal(vs.spmm(A, B, direction, "two_phase"), out)
+        A.destroy()
