@@ -182,14 +182,25 @@ vs_status vs_build_vcs(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_
  *   variant  see vs_variant (matters for misaligned directions only)
  *   stream   stream the product runs on
  *
- * B and out have the handle's dtype; vector loads are used when the width and
- * strides are multiples of 16 bytes and the pointers are 16-byte aligned.
+ * B and out have the handle's dtype, or both float64 with a float32 CSR or a
+ * VCS handle (float32 stored values, float64 products and sums; misaligned
+ * directions then need the transposed route).  Vector loads are used when the
+ * width and strides are multiples of 16 bytes and the pointers are 16-byte
+ * aligned.
  * w = 0 or an empty matrix returns VS_OK after writing zeros where out has
  * elements.  No allocation happens here for VS_ATOMIC, VS_TRANSPOSED and
  * aligned directions; the two-phase scheme may grow the handle's scratch on
  * first use with a new width (stream-ordered).  Calls on
  * the same handle must not overlap on the GPU (they share scratch).
  * VS_TRANSPOSED needs vs_attach_transpose first, else VS_ERR_INVALID.
+ * Errors: VS_ERR_INVALID (NULL handle or descriptor, unknown direction or
+ * variant, dtypes that do not match as above, B and out overlapping),
+ * VS_ERR_SHAPE (shapes that do not fit A), VS_ERR_LAYOUT (width axis not of
+ * stride 1, a stride smaller than the width), VS_ERR_UNSUPPORTED (float64
+ * operands with a float32 matrix on the two-phase or atomic route, a row
+ * stride of 2^32 bytes or more), VS_ERR_ALLOC / VS_ERR_CUDA from the runtime.
+ * A kernel whose bounded wait gave up marks the handle; vs_device_status
+ * reports it.
  */
 vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direction dir,
                   vs_variant variant, cudaStream_t stream);
