@@ -194,9 +194,9 @@ vs_status vs_build_vcs(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_
  * the same handle must not overlap on the GPU (they share scratch).
  * VS_TRANSPOSED needs vs_attach_transpose first, else VS_ERR_INVALID.
  * Errors: VS_ERR_INVALID (NULL handle or descriptor, unknown direction or
- * variant, dtypes that do not match as above, B and out overlapping),
- * VS_ERR_SHAPE (shapes that do not fit A), VS_ERR_LAYOUT (width axis not of
- * stride 1, a stride smaller than the width), VS_ERR_UNSUPPORTED (float64
+ * variant, dtypes that do not match as above), VS_ERR_SHAPE (shapes that
+ * do not fit A), VS_ERR_LAYOUT (width axis not of stride 1, a stride smaller
+ * than the width, B and out overlapping), VS_ERR_UNSUPPORTED (float64
  * operands with a float32 matrix on the two-phase or atomic route, a row
  * stride of 2^32 bytes or more), VS_ERR_ALLOC / VS_ERR_CUDA from the runtime.
  * A kernel whose bounded wait gave up marks the handle; vs_device_status
