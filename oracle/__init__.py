@@ -16,6 +16,13 @@ Functions and the passages they follow:
   the per-element error scale D = sum |a| |b|.
 * :func:`spmm_ab_rows`, :func:`spmm_ba_cols` -- the same for a sample of output
   rows (resp. columns), for matrices too large for a full product.
+* :func:`view_triples` -- the triples of a normalized view
+  diag(row_scale) g(A) diag(col_scale) ("Add CUDA transfer and matmul kernels
+  for the normalized views", "The layout stays compressed").
+* :func:`spmm_slices` -- the products over a stored layout on several host
+  threads (same page, "The kernels": whole slices per thread where the output
+  is aligned with the slices, per-thread private outputs merged in thread order
+  where it is not); the host cores' baseline.
 """
 from __future__ import annotations
 
@@ -49,8 +56,11 @@ def build(force: bool = False) -> str:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-           _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+           "-fopenmp", _SRC, "-o", tmp, "-lm"]
+    if subprocess.run(cmd).returncode != 0:
+        # no OpenMP runtime: the same source, one thread
+        cmd.remove("-fopenmp")
+        subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -74,6 +84,13 @@ def _configure(lib):
         f = getattr(lib, name)
         f.restype = None
         f.argtypes = [i64, i64, i32p, i32p, vp, vp, i64, i64, i64, vp, vp, vp, vp]
+    lib.or_view_triples.restype = ctypes.c_int
+    lib.or_view_triples.argtypes = [i64, i32p, i32p, vp, ctypes.c_int, vp, vp, vp]
+    lib.or_threads_available.restype = ctypes.c_int
+    lib.or_threads_available.argtypes = []
+    lib.or_spmm_slices.restype = ctypes.c_int
+    lib.or_spmm_slices.argtypes = [i64, i64, i32p, i32p, i32p, vp, ctypes.c_int, vp, i64, vp, vp,
+                                   ctypes.c_int]
     return lib
 
 
@@ -249,3 +266,58 @@ def spmm_ba_cols(n_cols: int, ti, tj, ta, Bt, sel):
     lib.or_spmm_ba_cols(n_cols, ti.size, _p(ti), _p(tj), _p(ta), _p(B), B.shape[1], w, sel.size,
                         _p(sel), _p(slot), _p(out), _p(D))
     return out, D
+
+
+MAPS = {"identity": 0, "log1p": 1, "sqrt": 2}
+
+
+def view_triples(ti, tj, ta, map: str = "identity", row_scale=None, col_scale=None):
+    """Triples of the view diag(row_scale) g(A) diag(col_scale): (ti, tj, a') with
+    a' = row_scale[i] * g(a) * col_scale[j] in float64 (None: all ones)."""
+    lib = _load()
+    ti, tj, ta = _i32(ti), _i32(tj), _f64(ta)
+    rs = None if row_scale is None else _f64(row_scale)
+    cs = None if col_scale is None else _f64(col_scale)
+    if rs is not None and ti.size and int(ti.max()) >= rs.size:
+        raise OracleError("row_scale shorter than the rows")
+    if cs is not None and tj.size and int(tj.max()) >= cs.size:
+        raise OracleError("col_scale shorter than the columns")
+    out = np.zeros(max(ta.size, 1), np.float64)
+    _check(lib.or_view_triples(ta.size, _p(ti), _p(tj), _p(ta), MAPS[map],
+                               None if rs is None else _p(rs), None if cs is None else _p(cs),
+                               _p(out)))
+    return ti, tj, out[:ta.size]
+
+
+def threads_available() -> int:
+    """Threads the threaded oracle products use by default (1 without OpenMP)."""
+    return int(_load().or_threads_available())
+
+
+def spmm_slices(ptr, idx, vals, X, aligned: bool, n_minor: int, value_ptr=None,
+                threads: int = 0):
+    """The product over a stored layout in the slice frame, on ``threads`` host
+    threads (0: all OpenMP offers).
+
+    ``ptr`` (n_major+1) indexes entries (CSR) or runs (VCS, with ``value_ptr``);
+    ``vals`` holds one value per entry (CSR) or per run (VCS).
+    aligned:   Y[s] = sum a X[t] over the entries (t, a) of slice s; X is n_minor x w.
+    misaligned: Y[t] = sum a X[s]; X is n_major x w, Y is n_minor x w.
+    Returns (Y, D), D = sum |a||x| per element.
+    """
+    lib = _load()
+    ptr, idx = _i32(ptr), _i32(idx)
+    vals = _f64(vals)
+    vp_ = None if value_ptr is None else _i32(value_ptr)
+    X = _f64(X)
+    n_major = ptr.size - 1
+    w = X.shape[1]
+    if X.shape[0] != (n_minor if aligned else n_major):
+        raise OracleError("X has the wrong number of rows for this frame")
+    n_out = n_major if aligned else n_minor
+    Y = np.zeros((n_out, w), np.float64)
+    D = np.zeros((n_out, w), np.float64)
+    _check(lib.or_spmm_slices(n_major, n_minor, _p(ptr), None if vp_ is None else _p(vp_),
+                              _p(idx), _p(vals), int(bool(aligned)), _p(X), w, _p(Y), _p(D),
+                              int(threads)))
+    return Y, D

@@ -33,6 +33,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define OR_OK 0
 #define OR_ERR_RANGE (-1)
@@ -300,4 +303,134 @@ void or_spmm_ba_cols(int64_t n_cols, int64_t nnz, const int32_t *ti, const int32
             D[s * w + c] += fabs(b) * fabs(a);
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Normalized views ("Add CUDA transfer and matmul kernels for the           */
+/* normalized views", "The layout stays compressed": a view applies a value  */
+/* transform and carries per-row and per-column statistics).  The view of A  */
+/* is V = diag(row_scale) . g(A) . diag(col_scale): entry (i, j, a) of A     */
+/* becomes (i, j, row_scale[i] * g(a) * col_scale[j]).                       */
+/*   map 0: g(a) = a;  map 1: g(a) = log(1 + a);  map 2: g(a) = sqrt(a).     */
+/* row_scale / col_scale may be NULL (all ones).  Returns OR_ERR_ARG for an  */
+/* unknown map.                                                              */
+/* ------------------------------------------------------------------------ */
+int or_view_triples(int64_t nnz, const int32_t *ti, const int32_t *tj, const double *ta,
+                    int map, const double *row_scale, const double *col_scale, double *out)
+{
+    if (map < 0 || map > 2) return OR_ERR_ARG;
+    for (int64_t k = 0; k < nnz; k++) {
+        double v = ta[k];
+        if (map == 1) v = log1p(v);
+        if (map == 2) v = sqrt(v);
+        if (row_scale) v = row_scale[ti[k]] * v;
+        if (col_scale) v = v * col_scale[tj[k]];
+        out[k] = v;
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The same products over a stored layout, on several host threads (the     */
+/* pages' host kernels: "Add CUDA transfer and matmul kernels ...", "The     */
+/* kernels" -- aligned directions take whole slices per thread, misaligned   */
+/* ones accumulate into per-thread private outputs that are then merged).    */
+/*                                                                          */
+/* Slice frame: a slice s is a stored major index; its entries (t, a) carry  */
+/* the minor index t.  `ptr` gives each slice's entry range (CSR), or its    */
+/* run range when `vptr` is given (VCS: run r holds entries vptr[r] ..       */
+/* vptr[r+1]-1, all with value vals[r]; otherwise vals[k] is entry k's).     */
+/*   aligned = 1:  Y[s, :] = sum over entries (t, a) of s of a * X[t, :]     */
+/*                 (X: n_minor x w, Y: n_major x w)                          */
+/*   aligned = 0:  Y[t, :] = sum over slices s, entries (t, a) of a * X[s, :] */
+/*                 (X: n_major x w, Y: n_minor x w)                          */
+/* Both row-major with row stride w.  D receives sum |a| |x| per element.    */
+/* Aligned: each output row is summed in entry order by one thread, exactly  */
+/* as the serial products above add it.  Misaligned: thread k of T takes the */
+/* slices [n_major k / T, n_major (k+1) / T) into a private Y_k; then        */
+/* Y = Y_0 + Y_1 + ... in thread order, so the result depends on T only.     */
+/* n_threads <= 0 means every thread OpenMP offers.  Returns OR_ERR_ALLOC    */
+/* when the private outputs cannot be allocated.                             */
+/* ------------------------------------------------------------------------ */
+int or_threads_available(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+int or_spmm_slices(int64_t n_major, int64_t n_minor, const int32_t *ptr, const int32_t *vptr,
+                   const int32_t *idx, const double *vals, int aligned, const double *X,
+                   int64_t w, double *Y, double *D, int n_threads)
+{
+    if (n_major < 0 || n_minor < 0 || w < 0) return OR_ERR_ARG;
+    int T = n_threads > 0 ? n_threads : or_threads_available();
+    if (T < 1) T = 1;
+    if (aligned) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(T)
+#endif
+        for (int64_t s = 0; s < n_major; s++) {
+            double *y = Y + s * w, *d = D + s * w;
+            for (int64_t c = 0; c < w; c++) { y[c] = 0.0; d[c] = 0.0; }
+            int64_t lo = ptr[s], hi = ptr[s + 1];
+            for (int64_t q = lo; q < hi; q++) {
+                /* CSR: q is an entry; VCS: q is a run covering vptr[q] .. vptr[q+1]-1 */
+                int64_t k0 = vptr ? vptr[q] : q, k1 = vptr ? vptr[q + 1] : q + 1;
+                double a = vals[q];
+                for (int64_t k = k0; k < k1; k++) {
+                    const double *x = X + (int64_t)idx[k] * w;
+                    for (int64_t c = 0; c < w; c++) {
+                        y[c] += a * x[c];
+                        d[c] += fabs(a) * fabs(x[c]);
+                    }
+                }
+            }
+        }
+        return OR_OK;
+    }
+    /* misaligned: private outputs per thread, merged in thread order */
+    size_t per = (size_t)(n_minor > 0 ? n_minor : 1) * (size_t)(w > 0 ? w : 1);
+    double *priv = (double *)calloc((size_t)T * per * 2, sizeof(double));
+    if (!priv) return OR_ERR_ALLOC;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static, 1) num_threads(T)
+#endif
+    for (int k = 0; k < T; k++) {
+        double *y = priv + (size_t)k * per * 2, *d = y + per;
+        int64_t s0 = n_major * k / T, s1 = n_major * (k + 1) / T;
+        for (int64_t s = s0; s < s1; s++) {
+            const double *x = X + s * w;
+            for (int64_t q = ptr[s]; q < ptr[s + 1]; q++) {
+                int64_t k0 = vptr ? vptr[q] : q, k1 = vptr ? vptr[q + 1] : q + 1;
+                double a = vals[q];
+                for (int64_t e = k0; e < k1; e++) {
+                    double *yt = y + (int64_t)idx[e] * w, *dt = d + (int64_t)idx[e] * w;
+                    for (int64_t c = 0; c < w; c++) {
+                        yt[c] += a * x[c];
+                        dt[c] += fabs(a) * fabs(x[c]);
+                    }
+                }
+            }
+        }
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(T)
+#endif
+    for (int64_t t = 0; t < n_minor; t++) {
+        for (int64_t c = 0; c < w; c++) {
+            double ys = 0.0, ds = 0.0;
+            for (int k = 0; k < T; k++) {
+                const double *y = priv + (size_t)k * per * 2;
+                ys += y[t * w + c];
+                ds += y[per + t * w + c];
+            }
+            Y[t * w + c] = ys;
+            D[t * w + c] = ds;
+        }
+    }
+    free(priv);
+    return OR_OK;
 }

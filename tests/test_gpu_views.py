@@ -1,7 +1,7 @@
 """Normalized views: products with diag(r) g(A) diag(c) in place of A, for the
 value maps and scalings of vs_spmm_view, every layout and direction, against
-the float64 oracle run on the mapped and scaled triples."""
-import numpy as np
+the float64 oracle's view of the matrix (oracle.view_triples) and its
+products."""
 import pytest
 import torch
 
@@ -14,9 +14,6 @@ from gpu_helpers import (PRODUCTS, TOL, aligned, assert_close, build, dense_oper
                          oracle_product, oracle_triples)
 
 pytestmark = pytest.mark.gpu
-
-G = {"identity": lambda v: v, "log1p": np.log1p, "sqrt": np.sqrt}
-
 
 @pytest.fixture(scope="module", autouse=True)
 def _cuda():
@@ -33,12 +30,8 @@ def _scales(coo, dtype, seed):
 
 def _view_triples(tri, gname, r, c):
     ti, tj, ta = tri
-    a = G[gname](np.asarray(ta, np.float64))
-    if r is not None:
-        a = a * r.double().numpy()[ti]
-    if c is not None:
-        a = a * c.double().numpy()[tj]
-    return ti, tj, a
+    return oracle.view_triples(ti, tj, ta, gname, None if r is None else r.double().numpy(),
+                               None if c is None else c.double().numpy())
 
 
 @pytest.mark.parametrize("gname", ["identity", "log1p", "sqrt"])

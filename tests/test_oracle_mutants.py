@@ -57,6 +57,21 @@ MUTANTS = {
     # or_spmm_ba_cols: the sampled columns drop the sign of A
     "ba_cols_sign_of_a": ("            out[s * w + c] += b * a;",
                           "            out[s * w + c] += b * fabs(a);"),
+    # or_view_triples: the row scaling indexed by the column (a transposed statistic)
+    "view_scale_index": ("        if (row_scale) v = row_scale[ti[k]] * v;",
+                         "        if (row_scale) v = row_scale[tj[k] < ti[k] ? tj[k] : ti[k]] * v;"),
+    # or_view_triples: log instead of log1p
+    "view_log_not_log1p": ("        if (map == 1) v = log1p(v);",
+                           "        if (map == 1) v = log(v > 0 ? v : 1.0);"),
+    # or_spmm_slices: the merge of private outputs leaves out the last thread
+    "slices_merge_drops_thread": ("            for (int k = 0; k < T; k++) {\n                const double *y = priv",
+                                  "            for (int k = 0; k + 1 < T; k++) {\n                const double *y = priv"),
+    # or_spmm_slices: a VCS run's value taken from the entry index (wrong array index)
+    "slices_value_by_entry": ("                for (int64_t k = k0; k < k1; k++) {\n                    const double *x = X + (int64_t)idx[k] * w;",
+                              "                for (int64_t k = k0; k < k1; k++) {\n                    a = vals[k < hi ? k : q];\n                    const double *x = X + (int64_t)idx[k] * w;"),
+    # or_spmm_slices: each thread's slice range ends one slice early
+    "slices_range_short": ("        int64_t s0 = n_major * k / T, s1 = n_major * (k + 1) / T;",
+                           "        int64_t s0 = n_major * k / T, s1 = n_major * (k + 1) / T - (n_major * (k + 1) / T > n_major * k / T);"),
 }
 
 
@@ -83,6 +98,11 @@ def _pin_battery():
     yield pins.test_duplicates_are_summed
     yield pins.test_vcs_and_csr_products_agree_on_workload
     yield pins.test_sampled_products_match_full
+    yield pins.test_golden_view_worked_example
+    yield pins.test_view_closed_forms
+    for threads in (1, 3, 8):
+        yield lambda threads=threads: pins.test_threaded_products_match_serial(threads)
+    yield pins.test_threaded_products_equal_dense_matmul_exactly
 
 
 def _failing_pins() -> int:

@@ -314,3 +314,115 @@ def test_sampled_products_match_full():
     sel = np.array([89, 0, 33])
     part, Dpart = oracle.spmm_ba_cols(90, r, c, v, Bt, sel)
     assert np.array_equal(part, full[:, sel].T) and np.array_equal(Dpart, Dfull[:, sel].T)
+
+
+# ----------------------------------------------------------------------------- views
+
+
+def test_golden_view_worked_example():
+    """view_triples against the hand-worked view example, every map, with both
+    scalings and with the row scaling alone."""
+    g = json.load(open(os.path.join(GOLDEN, "view_worked_example.json")))
+    ti, tj, ta = np.array(g["ti"]), np.array(g["tj"]), np.array(g["ta"])
+    r, c = np.array(g["row_scale"]), np.array(g["col_scale"])
+    for name, want in g["views"].items():
+        _, _, got = oracle.view_triples(ti, tj, ta, name, r, c)
+        np.testing.assert_allclose(got, want, rtol=1e-15, atol=0, err_msg=name)
+    for name, want in g["views_row_scale_only"].items():
+        _, _, got = oracle.view_triples(ti, tj, ta, name, r, None)
+        np.testing.assert_allclose(got, want, rtol=1e-15, atol=0, err_msg=name)
+    _, _, a = oracle.view_triples(ti, tj, ta, "sqrt", r, c)
+    out, _ = oracle.spmm_ab(g["n_rows"], g["n_cols"], ti, tj, a, np.array(g["B"]))
+    assert out.tolist() == g["sqrt_view_times_B"]
+
+
+def test_view_closed_forms():
+    """Identity without scalings returns the values; power-of-two scalings are
+    exact; the column scaling of A equals scaling the rows of B (and the row
+    scaling of A equals scaling the output rows) in a product."""
+    coo = W.make("tiny", seed=3)
+    ti, tj, ta = oracle.csr_triples(True, *oracle.csr_build(coo.n_rows, coo.n_cols, *_np(coo)))
+    assert np.array_equal(oracle.view_triples(ti, tj, ta)[2], ta)
+    rng = np.random.default_rng(5)
+    r = 2.0 ** rng.integers(-3, 4, coo.n_rows)
+    c = 2.0 ** rng.integers(-3, 4, coo.n_cols)
+    _, _, a = oracle.view_triples(ti, tj, ta, "identity", r, c)
+    assert np.array_equal(a, ta * r[ti] * c[tj])
+    B = rng.integers(-3, 4, (coo.n_cols, 5)).astype(np.float64)
+    rs = rng.integers(1, 4, coo.n_rows).astype(np.float64)
+    cs = rng.integers(1, 4, coo.n_cols).astype(np.float64)
+    _, _, av = oracle.view_triples(ti, tj, ta, "identity", rs, cs)
+    got, _ = oracle.spmm_ab(coo.n_rows, coo.n_cols, ti, tj, av, B)
+    want = rs[:, None] * (_dense(coo.n_rows, coo.n_cols, ti, tj, ta) @ (cs[:, None] * B))
+    assert np.array_equal(got, want)  # small integers: every sum is exact
+    # the maps against numpy's own log1p / sqrt on the stored values
+    for name, f in (("log1p", np.log1p), ("sqrt", np.sqrt)):
+        np.testing.assert_allclose(oracle.view_triples(ti, tj, ta, name)[2], f(ta), rtol=1e-15)
+
+
+# ----------------------------------------------------------------------------- threaded products
+
+
+def _frames(coo):
+    """(label, ptr, idx, vals, value_ptr, n_major, n_minor, triples) of the four layouts."""
+    r, c, v = _np(coo)
+    out = []
+    for major in ("row", "col"):
+        maj, mnr = (r, c) if major == "row" else (c, r)
+        nm, nn = (coo.n_rows, coo.n_cols) if major == "row" else (coo.n_cols, coo.n_rows)
+        p, i, vv = oracle.csr_build(nm, nn, maj, mnr, v)
+        out.append((f"csr/{major}", p, i, vv, None, nm, nn,
+                    oracle.csr_triples(major == "row", p, i, vv)))
+        mp, vals, vp, ind = oracle.vcs_build(nm, nn, maj, mnr, v)
+        out.append((f"vcs/{major}", mp, ind, vals, vp, nm, nn,
+                    oracle.vcs_triples(major == "row", mp, vals, vp, ind)))
+    return out
+
+
+def _serial_frame(coo, major_is_row, aligned, tri, X):
+    """The serial products of the triples, in the slice frame of a layout."""
+    ti, tj, ta = tri
+    # slice frame: aligned products with a row major are A @ X; with a column
+    # major they are A^T @ X (= (X^T A)^T); misaligned ones the other way round
+    if major_is_row == aligned:
+        return oracle.spmm_ab(coo.n_rows, coo.n_cols, ti, tj, ta, X)
+    out, D = oracle.spmm_ba(coo.n_rows, coo.n_cols, ti, tj, ta, np.ascontiguousarray(X.T))
+    return out.T, D.T
+
+
+@pytest.mark.parametrize("threads", [1, 3, 8])
+def test_threaded_products_match_serial(threads):
+    """Aligned frames: bit-identical to the serial products (each output row is
+    summed in entry order either way).  Misaligned frames: within 1e-12 * D of
+    the serial products, and bit-identical on one thread."""
+    coo = W.make("tiny", seed=7)
+    rng = np.random.default_rng(threads)
+    for label, p, i, vals, vp, nm, nn, tri in _frames(coo):
+        row = label.endswith("row")
+        for aligned in (True, False):
+            X = rng.standard_normal((nn if aligned else nm, 6))
+            got, gD = oracle.spmm_slices(p, i, vals, X, aligned, nn, vp, threads)
+            want, wD = _serial_frame(coo, row, aligned, tri, X)
+            if aligned or threads == 1:
+                assert np.array_equal(got, want), (label, aligned)
+                assert np.array_equal(gD, wD), (label, aligned)
+            else:
+                assert np.all(np.abs(got - want) <= 1e-12 * wD), (label, aligned)
+                assert np.allclose(gD, wD, rtol=1e-12, atol=0), (label, aligned)
+
+
+def test_threaded_products_equal_dense_matmul_exactly():
+    """Small-integer operands: every partial sum is exact, so each frame equals
+    numpy's integer matmul of the dense matrix bit for bit, at any thread count."""
+    coo = W.random_coo(300, 170, 4000, seed=12, duplicates=True, sort=False)
+    A = _dense(coo.n_rows, coo.n_cols, coo.rows.numpy(), coo.cols.numpy(),
+               coo.vals.numpy().astype(np.float64))
+    rng = np.random.default_rng(1)
+    for label, p, i, vals, vp, nm, nn, _ in _frames(coo):
+        M = A if label.endswith("row") else A.T          # n_major x n_minor
+        for aligned in (True, False):
+            X = rng.integers(-4, 5, (nn if aligned else nm, 5)).astype(np.float64)
+            want = M @ X if aligned else M.T @ X
+            for threads in (1, 4, 7):
+                got, _ = oracle.spmm_slices(p, i, vals, X, aligned, nn, vp, threads)
+                assert np.array_equal(got, want), (label, aligned, threads)
