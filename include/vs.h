@@ -229,7 +229,9 @@ vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direct
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array, which keeps whatever the last call
  * left in it; calls whose work overlaps on the GPU (other streams, other
- * threads) race on it and must be serialised by the caller.
+ * threads) race on it and must be serialised by the caller.  The looked-up
+ * address is kept for the life of the process, so resetting a device
+ * (cudaDeviceReset) while the library is loaded is not supported.
  */
 vs_status vs_spmm_noalloc(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direction dir,
                           cudaStream_t stream);
@@ -329,6 +331,21 @@ vs_status vs_transpose(vs_handle A, cudaStream_t stream, vs_handle *out);
  */
 vs_status vs_scale_entries(vs_handle A, const void *factors, cudaStream_t stream,
                            vs_handle *out);
+
+/*
+ * vs_force_group_size -- test hook for the group size ("Regridder", "Tests":
+ * every group size from 1 to 32 must reproduce the dense product).  From this
+ * call on, the gathers over A, and over its exact transpose (attached now or
+ * later), give every slice g logical partial sums instead of the g that the
+ * matrix rule picks (the largest power of two <= the mean entries per slice,
+ * at most 32).  The summation order then follows the forced g: results stay
+ * within the tolerance of the exact product, repeat bit for bit, and give a
+ * column the same bits alone or in a batch, but their last bits may differ
+ * from those under the rule.  g = 0 restores the rule.  Host-side only:
+ * call it between products, not while another host thread runs one on A.
+ *   g  0, 1, 2, 4, 8, 16 or 32 (VS_ERR_INVALID otherwise)
+ */
+vs_status vs_force_group_size(vs_handle A, int32_t g);
 
 /* vs_info -- shape, layout and matrix-only kernel parameters of A. */
 vs_status vs_info(vs_handle A, vs_info_t *info);

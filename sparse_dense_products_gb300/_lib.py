@@ -93,13 +93,14 @@ def load() -> ctypes.CDLL:
         lib.vs_test_stall_producers.argtypes = [i32]
         lib.vs_test_stall_producers.restype = None
         lib.vs_scale_entries.argtypes = [H, vp, vp, ctypes.POINTER(H)]
+        lib.vs_force_group_size.argtypes = [H, ctypes.c_int32]
         lib.vs_info.argtypes = [H, ctypes.POINTER(Info)]
         lib.vs_export.argtypes = [H, ctypes.POINTER(Arrays)]
         lib.vs_handle_bytes.argtypes = [H, ctypes.POINTER(i64), ctypes.POINTER(i64)]
         lib.vs_destroy.argtypes = [H]
         for f in ("vs_build_csr", "vs_build_vcs", "vs_spmm", "vs_spmm_host", "vs_spmm_noalloc",
                   "vs_spmm_view",
-                  "vs_attach_transpose", "vs_transpose", "vs_scale_entries", "vs_gather_floor", "vs_device_status",
+                  "vs_attach_transpose", "vs_transpose", "vs_scale_entries", "vs_force_group_size", "vs_gather_floor", "vs_device_status",
                   "vs_info", "vs_export", "vs_handle_bytes", "vs_destroy"):
             getattr(lib, f).restype = i32
         lib.vs_status_string.argtypes = [i32]

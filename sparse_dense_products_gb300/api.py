@@ -121,6 +121,12 @@ class SparseMatrix:
                                           ctypes.byref(h)))
         return SparseMatrix(h.value, self.shape, self.device)
 
+    def force_group_size(self, g: int) -> "SparseMatrix":
+        """``vs_force_group_size``: test hook fixing the group size g of this
+        matrix's gathers (1, 2, 4, ..., 32; 0 restores the matrix rule)."""
+        L.check(L.load().vs_force_group_size(self.handle, int(g)))
+        return self
+
     def destroy(self) -> None:
         if self._h:
             L.check(L.load().vs_destroy(self._h))

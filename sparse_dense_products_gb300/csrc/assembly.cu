@@ -619,13 +619,7 @@ vs_status prepare_matrix(Matrix &m, cudaStream_t s) {
     return m.layout == VS_LAYOUT_VCS ? vptr[ptr[sl]] : ptr[sl];
   };
 
-  // group size g: the largest power of two <= the mean entries per slice, in [1, 32]
-  int g = 1;
-  if (m.n_major > 0) {
-    const int64_t mean = m.nnz / m.n_major;
-    while (g * 2 <= mean && g < 32) g *= 2;
-  }
-  m.g = g;
+  m.g = group_size_rule(m.nnz, m.n_major);
   {
     int dev = 0;
     VS_CUDA(cudaGetDevice(&dev));

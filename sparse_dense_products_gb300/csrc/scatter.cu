@@ -796,6 +796,9 @@ vs_status two_phase_static_typed(const Matrix &m, DenseView X, DenseView Y, int6
     const int64_t per_col = (int64_t)C * n_t * (int64_t)sizeof(T);
     wmax = std::min<int64_t>(kMaxBlockWidth, (int64_t)kStaticScratchBytes / std::max<int64_t>(per_col, 1));
     if (wmax >= VW) wmax = wmax / VW * VW;
+    // C is bounded at build time so that C copies of the output stay within
+    // 64 MiB at width 64, i.e. at most 1 MiB per column: this rejection is a
+    // guard, not a path a handle built here can reach
     if (wmax < 1) {
       set_error("vs_spmm_noalloc: the partial sums need " + std::to_string(per_col) +
                 " bytes per column; the static scratch holds " +

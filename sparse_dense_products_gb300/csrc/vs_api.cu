@@ -635,7 +635,18 @@ vs_status vs_attach_transpose(vs_handle A, cudaStream_t stream) {
     set_error(msg);
     return st;
   }
+  if (A->forced_g) t->g = A->forced_g;
   A->T = t;
+  return VS_OK;
+}
+
+vs_status vs_force_group_size(vs_handle A, int32_t g) {
+  if (!valid_handle(A)) return invalid("NULL handle");
+  if (g != 0 && g != 1 && g != 2 && g != 4 && g != 8 && g != 16 && g != 32)
+    return invalid("group size must be 0, 1, 2, 4, 8, 16 or 32");
+  A->forced_g = g;
+  for (Matrix *m : {&A->A, A->T})
+    if (m) m->g = g ? g : group_size_rule(m->nnz, m->n_major);
   return VS_OK;
 }
 

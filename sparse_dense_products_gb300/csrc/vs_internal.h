@@ -113,6 +113,18 @@ struct Scratch {
   void release();
 };
 
+// Group size rule ("Regridder", "How it is built": as many threads as an
+// average slice has entries, up to a warp): the largest power of two <= the
+// mean entries per slice, clamped to [1, 32].
+inline int group_size_rule(int64_t nnz, int64_t n_major) {
+  int g = 1;
+  if (n_major > 0) {
+    const int64_t mean = nnz / n_major;
+    while (g * 2 <= mean && g < 32) g *= 2;
+  }
+  return g;
+}
+
 void free_matrix(Matrix &m);
 vs_status dev_alloc(void **p, size_t bytes);
 vs_status share_index_arrays(Matrix &m);
@@ -128,6 +140,7 @@ struct vs_handle_s {
   int *host_flags = nullptr;       // pinned: the failure flags of A and T, read back by vs_spmm_host
   vs::Scratch view_vals, view_tvals, view_X;  // normalized views: mapped values, scaled X
   vs::Scratch floor_sink;                      // vs_gather_floor's per-thread sums
+  int forced_g = 0;                            // vs_force_group_size (0: the matrix rule)
 };
 
 namespace vs {

@@ -1,8 +1,9 @@
 """vs_spmm_host: the product with B and out in host memory (the end-to-end
-path of the benchmark) equals the device product bit for bit, for pinned and
-pageable buffers (a pinned output of a gather is written in place by the
-kernel, a pageable one is staged and copied back), pitched and strided host
-views, and leaves host memory outside the logical output untouched."""
+path of the benchmark) matches the float64 oracle within the tolerance and
+equals the device product bit for bit, for pinned and pageable buffers (a
+pinned output of a gather is written in place by the kernel, a pageable one is
+staged and copied back), pitched and strided host views, and leaves host memory
+outside the logical output untouched."""
 import pytest
 import torch
 
@@ -10,7 +11,8 @@ import sparse_dense_products_gb300 as vs
 from sparse_dense_products_gb300 import build as vs_build
 from sparse_dense_products_gb300 import workloads as W
 
-from gpu_helpers import PRODUCTS, build, dense_operand
+from gpu_helpers import (PRODUCTS, TOL, assert_close, build, dense_operand, gpu_out_rows,
+                         oracle_product, oracle_triples)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +39,8 @@ def test_host_operands_match_device_product(layout, major, direction, w, pad, pi
     coo = W.random_coo(900, 700, 40_000, seed=61, values="counts", sort=False)
     A = build(coo, layout, major)
     A.attach_transpose()
-    B, _ = dense_operand(coo, direction, w, torch.float32, seed=3)
+    B, Bt = dense_operand(coo, direction, w, torch.float32, seed=3)
+    ref, D = oracle_product(coo, oracle_triples(coo, layout, major), direction, Bt)
     want = vs.spmm(A, B, direction).cpu()
     if direction == "A@B":
         Bh = B.cpu()
@@ -49,6 +52,8 @@ def test_host_operands_match_device_product(layout, major, direction, w, pad, pi
         Bh = Bh.t()
     big, out = _host_out(A, w, direction, torch.float32, pin, pad)
     vs.spmm_host(A, Bh, direction, "deterministic", out=out)
+    assert_close(gpu_out_rows(out, direction), ref, D, TOL[torch.float32],
+                 f"host {layout}/{major} {direction} w={w} pin={pin}")
     assert torch.equal(out, want)
     if pad:
         rest = big[:, w:] if direction == "A@B" else big[w:, :]
@@ -59,10 +64,12 @@ def test_host_operands_match_device_product(layout, major, direction, w, pad, pi
 def test_host_operands_mixed_precision():
     coo = W.random_coo(500, 400, 20_000, seed=62, values="counts", sort=False)
     A = build(coo, "vcs", "row")
-    B, _ = dense_operand(coo, "A@B", 16, torch.float64, seed=4)
+    B, Bt = dense_operand(coo, "A@B", 16, torch.float64, seed=4)
+    ref, D = oracle_product(coo, oracle_triples(coo, "vcs", "row"), "A@B", Bt)
     want = vs.spmm(A, B, "A@B").cpu()
     got = vs.spmm_host(A, B.cpu().pin_memory(), "A@B", "deterministic")
     assert got.dtype == torch.float64 and torch.equal(got, want)
+    assert_close(gpu_out_rows(got, "A@B"), ref, D, TOL[torch.float64], "host mixed")
     A.destroy()
 
 
@@ -73,13 +80,15 @@ def test_host_operands_misaligned_variants(variant):
     coo = W.random_coo(700, 500, 30_000, seed=63, values="counts", sort=False)
     A = build(coo, "vcs", "row")
     A.attach_transpose()
-    B, _ = dense_operand(coo, "B@A", 16, torch.float32, seed=5)
+    B, Bt = dense_operand(coo, "B@A", 16, torch.float32, seed=5)
+    ref, D = oracle_product(coo, oracle_triples(coo, "vcs", "row"), "B@A", Bt)
     want = vs.spmm(A, B, "B@A", variant).cpu()
     Bh = B.cpu().t().contiguous().t()            # width-contiguous, pageable
     # a pinned, width-contiguous output inside a taller NaN-filled buffer
     big = torch.empty(coo.n_cols, 16 + 2, pin_memory=True).fill_(float("nan")).t()
     out = big[:16, :]
     vs.spmm_host(A, Bh, "B@A", variant, out=out)
+    assert_close(gpu_out_rows(out, "B@A"), ref, D, TOL[torch.float32], f"host B@VCSR {variant}")
     assert torch.equal(out, want)
     assert torch.isnan(big[16:, :]).all(), "host memory outside the output was written"
     A.destroy()

@@ -77,3 +77,40 @@ def test_noalloc_matches_vs_spmm_twice(name, layout, major, direction, w):
         assert np.array_equal(got, ref_rows), f"call {call}: bits differ from vs_spmm"
         assert np.all(np.abs(got - want) <= TOL[torch.float32] * D)
     A.destroy()
+
+
+def test_noalloc_on_a_fresh_handle_allocates_nothing():
+    """On a handle that has never run vs_spmm, two vs_spmm_noalloc calls of a
+    two-phase product leave the handle's scratch and the device's free memory
+    unchanged, and match vs_spmm on a second handle of the same matrix bit for
+    bit (and the oracle within the tolerance)."""
+    coo = W.random_coo(3000, 2500, 200_000, seed=22, values="counts", duplicates=True,
+                       sort=False)
+    direction, w = "B@A", 16
+    B, Bt = dense_operand(coo, direction, w, torch.float32, seed=6)
+    # a first call on another handle loads the library's module (and its
+    # static array) before anything is measured
+    warm = build(coo, "vcs", "row")
+    _noalloc(warm, B, vs.empty_out(warm, w, direction), direction)
+    warm.destroy()
+    A = build(coo, "vcs", "row")
+    outs = [vs.empty_out(A, w, direction) for _ in range(2)]
+    torch.cuda.synchronize()
+    _, scratch0 = A.nbytes()
+    free0, _ = torch.cuda.mem_get_info()
+    for out in outs:
+        _noalloc(A, B, out, direction)
+    torch.cuda.synchronize()
+    _, scratch1 = A.nbytes()
+    free1, _ = torch.cuda.mem_get_info()
+    assert scratch1 == scratch0, (scratch0, scratch1)
+    assert free1 == free0, (free0, free1)
+    R = build(coo, "vcs", "row")
+    ref = gpu_out_rows(vs.spmm(R, B, direction, "deterministic"), direction)
+    want, D = oracle_product(coo, oracle_triples(coo, "vcs", "row"), direction, Bt)
+    for out in outs:
+        got = gpu_out_rows(out, direction)
+        assert np.array_equal(got, ref)
+        assert np.all(np.abs(got - want) <= TOL[torch.float32] * D)
+    A.destroy()
+    R.destroy()
