@@ -190,38 +190,70 @@ def algorithmic_bytes(A, n_x_rows: int, n_y_rows: int, w: int, es: int = 4) -> i
 # ------------------------------------------------------------------ CPU oracle timing
 
 
-def oracle_prepare(coo):
-    """The oracle's own layouts of the workload, expanded to triples (not timed)."""
-    import oracle
-
-    r, c, v = coo.rows.numpy(), coo.cols.numpy(), coo.vals.numpy()
-    trip = {}
-    trip[("vcs", "row")] = oracle.vcs_triples(True, *oracle.vcs_build(coo.n_rows, coo.n_cols, r, c, v))
-    trip[("vcs", "col")] = oracle.vcs_triples(False, *oracle.vcs_build(coo.n_cols, coo.n_rows, c, r, v))
-    p, i, vv = oracle.csr_build(coo.n_rows, coo.n_cols, r, c, v)
-    trip[("csr", "row")] = oracle.csr_triples(True, p, i, vv)
-    return trip
+def host_cores() -> int:
+    """Cores this process may run on (the affinity mask), for the threaded oracle."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover - non-Linux hosts
+        return os.cpu_count() or 1
 
 
-def run_oracle_sample(trip, coo, Bab, Bba_rows, budget_s: float):
-    """Times the oracle's six products, repeated until `budget_s` seconds have passed."""
+def oracle_layouts(coo):
+    """The oracle's own stored layouts of the workload, per (layout, major): ptr,
+    idx, float64 values (per entry for CSR, per run for VCS), value_ptr or None,
+    n_minor.  Built once, not timed."""
     import numpy as np
     import oracle
 
-    Bba = np.ascontiguousarray(Bba_rows.T)
+    r, c, v = coo.rows.numpy(), coo.cols.numpy(), coo.vals.numpy()
+    out = {}
+    for major in ("row", "col"):
+        maj, mnr = (r, c) if major == "row" else (c, r)
+        nm, nn = (coo.n_rows, coo.n_cols) if major == "row" else (coo.n_cols, coo.n_rows)
+        mp, vals, vp, ind = oracle.vcs_build(nm, nn, maj, mnr, v)
+        out[("vcs", major)] = (mp, ind, vals.astype(np.float64), vp, nn)
+        if major == "row":
+            p, i, vv = oracle.csr_build(nm, nn, maj, mnr, v)
+            out[("csr", major)] = (p, i, vv.astype(np.float64), None, nn)
+    return out
+
+
+def run_oracle_sample(lays, Bab, Bba_rows, budget_s: float, threads: int):
+    """Times the oracle's six products (threaded layout loops, slice frame) on
+    `threads` host threads, repeated until `budget_s` seconds have passed.
+    Bab is B of the A@B products (n_cols x w); Bba_rows is B^T of the B@A
+    products (n_rows x w)."""
+    import oracle
+
     t0 = time.perf_counter()
     reps = 0
     while True:
         for _, layout, major, direction in PRODUCTS:
-            ti, tj, ta = trip[(layout, major)]
-            if direction == "A@B":
-                oracle.spmm_ab(coo.n_rows, coo.n_cols, ti, tj, ta, Bab)
-            else:
-                oracle.spmm_ba(coo.n_rows, coo.n_cols, ti, tj, ta, Bba)
+            ptr, idx, vals, vp, n_minor = lays[(layout, major)]
+            aligned = (direction == "A@B") == (major == "row")
+            X = Bab if direction == "A@B" else Bba_rows
+            oracle.spmm_slices(ptr, idx, vals, X, aligned, n_minor, vp, threads)
         reps += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     return reps, time.perf_counter() - t0
+
+
+def cpu_baseline_leg(coo, Bab, Bba_rows, step_bytes: int, seconds: float):
+    """The float64 oracle on the host cores: all cores of the affinity mask (the
+    reported value) and one core beside it, each for about `seconds`."""
+    lays = oracle_layouts(coo)
+    cores = host_cores()
+    r1, s1 = run_oracle_sample(lays, Bab, Bba_rows, seconds / 3, 1)
+    rn, sn = run_oracle_sample(lays, Bab, Bba_rows, seconds, cores)
+    return {"value": round(step_bytes * rn / sn / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"the six float64 oracle products over the oracle's own layouts of the full "
+                      f"workload on {cores} threads (whole slices per thread for aligned "
+                      f"products, private outputs merged in thread order for misaligned ones), "
+                      f"{rn} pass(es) in {sn:.1f} s",
+            "single_core": {"value": round(step_bytes * r1 / s1 / 1e9, 4), "unit": "GB/s",
+                            "cores": 1, "sample": f"{r1} pass(es) in {s1:.1f} s"}}
 
 
 def layout_bytes_host(coo):
@@ -261,13 +293,14 @@ def reference_arm(args):
     Bba_rows = W.dense(coo.n_rows, WIDTH, seed=2, device=gen).double().cpu().numpy()
     per = layout_bytes_host(coo)
     total_bytes = sum(per)
-    trip = oracle_prepare(coo)
-    # warm-up steps, then timed steps; one step = the six oracle products
+    lays = oracle_layouts(coo)
+    cores = host_cores()
+    # warm-up steps, then timed steps; one step = the six oracle products on all cores
     for _ in range(args.warmup):
-        run_oracle_sample(trip, coo, Bab, Bba_rows, 0.0)
+        run_oracle_sample(lays, Bab, Bba_rows, 0.0, cores)
     reps, secs = 0, 0.0
     for _ in range(args.steps):
-        r_, s_ = run_oracle_sample(trip, coo, Bab, Bba_rows, 0.0)
+        r_, s_ = run_oracle_sample(lays, Bab, Bba_rows, 0.0, cores)
         reps += r_
         secs += s_
     gbs = total_bytes * reps / secs / 1e9
@@ -279,13 +312,216 @@ def reference_arm(args):
         "config": {"workload": "main: 60000x2000 count matrix, %d nnz, width 16, six products "
                                "(VCSR@B VCSC@B B@VCSR B@VCSC CSR@B B@CSR), float64 oracle" % coo.nnz,
                    "l2": "n/a (host)", "generated_on": gen},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "full workload, six float64 oracle products per step"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "full workload, six float64 oracle products per step over the "
+                                   "oracle's own layouts, on every core of the affinity mask"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ------------------------------------------------------------------ GPU helpers
+
+
+def bit_repeatability(torch, fn, reps: int, column_fn=None, columns=()):
+    """Runs fn() `reps` times; counts the output values whose bits differ from the
+    first result in at least one repeat, and (with column_fn) the values of each
+    listed column computed alone whose bits differ from the same column of the
+    batch.  fn returns a 2-D tensor whose second axis is the width."""
+    first = fn().clone()
+    bits = first.view(torch.int64 if first.dtype == torch.float64 else torch.int32)
+    differ = torch.zeros_like(first, dtype=torch.bool)
+    reps_differing = 0
+    for _ in range(reps - 1):
+        o = fn()
+        d = o.view(bits.dtype) != bits
+        differ |= d
+        reps_differing += int(bool(d.any()))
+    res = {"reps": reps, "values": int(first.numel()),
+           "values_differing_in_a_repeat": int(differ.sum()),
+           "repeats_differing": reps_differing}
+    if column_fn is not None:
+        alone = {}
+        for c in columns:
+            a = column_fn(c).reshape(-1)
+            alone[str(c)] = int((a.view(bits.dtype) != bits[:, c].contiguous()).sum())
+        res["column_alone_values_differing"] = alone
+    torch.cuda.synchronize()
+    return res
+
+
+def time_product_set(vs, torch, coo, handles, specs, width: int, dtype, reps: int, timed,
+                     layout_bytes, seed: int = 1):
+    """Times each (name, layout, major, direction, variant) of `specs` at `width`
+    on the workload `coo` (device tensors).  Returns {name/variant: {ms, GBs,
+    frac_of_measured, frac_of_8TBs, bytes}}; a product's bytes are the stored
+    layout it streams (the other-major layout for a misaligned product run over
+    the transpose), B read once and out written once."""
+    from sparse_dense_products_gb300 import workloads as W
+
+    es = 8 if dtype == torch.float64 else 4
+    peak, _ = _peaks()
+    dev = coo.rows.device
+    Bab = W.dense(coo.n_cols, width, seed=seed, device=dev, dtype=dtype)
+    Bt = W.dense(coo.n_rows, width, seed=seed + 1, device=dev, dtype=dtype)
+    out = {}
+    for name, layout, major, direction, variant in specs:
+        A = handles[(layout, major)]
+        B = Bab if direction == "A@B" else Bt.t()
+        o = vs.empty_out(A, width, direction, dtype=dtype)
+        aligned = (direction == "A@B") == (major == "row")
+        m = major if aligned or variant not in ("deterministic", "transposed") else \
+            ("col" if major == "row" else "row")
+        nb = int(layout_bytes[(layout, m)] + (coo.n_rows + coo.n_cols) * width * es)
+        vs.spmm(A, B, direction, variant, out=o)
+        ts = timed(lambda: vs.spmm(A, B, direction, variant, out=o), reps)
+        ms = statistics.median(ts)
+        out[f"{name}/{variant}"] = {"ms": round(ms, 5), "GBs": round(nb / ms / 1e6, 1),
+                                    "frac_of_measured": round(nb / ms / 1e6 / peak, 4),
+                                    "frac_of_8TBs": round(nb / ms / 1e6 / NOMINAL_HBM_GBS, 4),
+                                    "bytes": nb}
+    del Bab, Bt
+    return out
+
+
+def cusparse_times(torch, coo_dev, handles, width: int, dtype, reps: int, timed, ours: dict,
+                   seed: int = 1):
+    """torch's CSR matmul (cuSPARSE SpMM) on the index-sorted CSR (CSR@B) and on
+    the CSR of the exact transpose (B@CSR), beside our deterministic times."""
+    import warnings
+
+    from sparse_dense_products_gb300 import workloads as W
+    import sparse_dense_products_gb300 as vs
+
+    warnings.filterwarnings("ignore", message="Sparse CSR tensor support is in beta")
+    res = {}
+    try:
+        dev = coo_dev.rows.device
+        A = handles[("csr", "row")]
+        a = A.arrays()
+        A_csr = torch.sparse_csr_tensor(a["ptr"], a["indices"], a["values"].to(dtype),
+                                        (coo_dev.n_rows, coo_dev.n_cols))
+        with vs.build_csr(coo_dev.cols, coo_dev.rows, coo_dev.vals, (coo_dev.n_cols, coo_dev.n_rows),
+                          "row") as hT:
+            t = hT.arrays()
+        AT_csr = torch.sparse_csr_tensor(t["ptr"], t["indices"], t["values"].to(dtype),
+                                         (coo_dev.n_cols, coo_dev.n_rows))
+        Bab = W.dense(coo_dev.n_cols, width, seed=seed, device=dev, dtype=dtype)
+        Bt = W.dense(coo_dev.n_rows, width, seed=seed + 1, device=dev, dtype=dtype)
+        for name, Am, X in (("CSR@B", A_csr, Bab), ("B@CSR", AT_csr, Bt)):
+            torch.mm(Am, X)
+            ms = statistics.median(timed(lambda: torch.mm(Am, X), reps))
+            entry = {"ms": round(ms, 5)}
+            key = f"{name}/deterministic"
+            if key in ours:
+                entry["ours_over_cusparse_time"] = round(ours[key]["ms"] / ms, 3)
+            res[name] = entry
+        del A_csr, AT_csr, Bab, Bt
+    except Exception as exc:  # reported, never fatal: a comparison, not the path
+        res = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
+    return res
+
+
+def build_handles(vs, coo, layouts, attach: bool = True):
+    """Handles of the workload for each (layout, major), transposes attached."""
+    hs = {}
+    for layout, major in layouts:
+        fn = vs.build_vcs if layout == "vcs" else vs.build_csr
+        hs[(layout, major)] = fn(coo.rows, coo.cols, coo.vals, (coo.n_rows, coo.n_cols), major)
+        if attach:
+            hs[(layout, major)].attach_transpose()
+    return hs
+
+
+def layout_bytes_of(handles, coo):
+    """Stored-layout bytes of each (layout, major) a product may stream; CSC from CSR."""
+    lb = {k: h.nbytes()[0] for k, h in handles.items()}
+    if ("csr", "row") in lb and ("csr", "col") not in lb:
+        lb[("csr", "col")] = lb[("csr", "row")] - 4 * coo.n_rows + 4 * coo.n_cols
+    return lb
+
+
+def extra_workloads(vs, torch, dev, timed, reps: int, log):
+    """The regridding-shaped, large and skewed workloads: ms, GB/s and fraction
+    of the measured HBM copy per product, deterministic and atomic variants,
+    and cuSPARSE beside them."""
+    from sparse_dense_products_gb300 import workloads as W
+
+    res = {}
+    peak, peak_kind = _peaks()
+    # regridding-shaped: backprojection rows of 2-4 entries and their exact
+    # transpose (the forward direction), float32 and float64, widths 1, 4, 32
+    t0 = time.perf_counter()
+    for dtype, tag in ((torch.float32, "f32"), (torch.float64, "f64")):
+        coo = W.make("regrid", seed=0, device=dev, dtype=dtype)
+        hs = build_handles(vs, coo, [("csr", "row")])
+        lb = layout_bytes_of(hs, coo)
+        for w in (1, 4, 32):
+            specs = [("CSR@B", "csr", "row", "A@B", "deterministic"),
+                     ("B@CSR", "csr", "row", "B@A", "deterministic"),
+                     ("B@CSR", "csr", "row", "B@A", "atomic")]
+            times = time_product_set(vs, torch, coo, hs, specs, w, dtype, reps, timed, lb)
+            times["cusparse"] = cusparse_times(torch, coo, hs, w, dtype, reps, timed, times)
+            res.setdefault("regrid", {})[f"{tag}/w{w}"] = times
+        res["regrid"][f"{tag}/nnz"] = coo.nnz
+        res["regrid"][f"{tag}/group_size"] = hs[("csr", "row")].info()["group_size"]
+        for h in hs.values():
+            h.destroy()
+        del coo
+    log(f"regrid done in {time.perf_counter() - t0:.1f} s")
+    # large: 1,000,000 x 20,000, ~200M nonzeros, the four VCS directions, w 8 and 32
+    t0 = time.perf_counter()
+    coo = W.make("large", seed=0, device=dev)
+    hs = build_handles(vs, coo, [("vcs", "row"), ("vcs", "col")])
+    hs[("csr", "row")] = vs.build_csr(coo.rows, coo.cols, coo.vals, (coo.n_rows, coo.n_cols), "row")
+    lb = layout_bytes_of(hs, coo)
+    large = {"nnz": coo.nnz, "runs_vcsr": hs[("vcs", "row")].info()["n_runs"],
+             "runs_vcsc": hs[("vcs", "col")].info()["n_runs"]}
+    for w in (8, 32):
+        specs = [("VCSR@B", "vcs", "row", "A@B", "deterministic"),
+                 ("VCSC@B", "vcs", "col", "A@B", "deterministic"),
+                 ("VCSC@B", "vcs", "col", "A@B", "atomic"),
+                 ("B@VCSR", "vcs", "row", "B@A", "deterministic"),
+                 ("B@VCSR", "vcs", "row", "B@A", "atomic"),
+                 ("B@VCSC", "vcs", "col", "B@A", "deterministic")]
+        times = time_product_set(vs, torch, coo, hs, specs, w, torch.float32, reps, timed, lb)
+        times["cusparse"] = cusparse_times(torch, coo, hs, w, torch.float32, reps, timed, {})
+        large[f"w{w}"] = times
+    det = {k: v for k, v in large["w32"].items() if k.endswith("/deterministic")}
+    dom = max(det, key=lambda k: det[k]["ms"])
+    name = dom.split("/")[0]
+    traffic = recorded_profile("large:" + name)
+    large["roofline"] = {"bound": "hbm", "kernel": dom + " w=32", "achieved": det[dom]["GBs"],
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": det[dom]["frac_of_measured"],
+                         "traffic": None if traffic is None else int(traffic),
+                         "traffic_note": "DRAM bytes per launch scaled from an ncu capture of "
+                                         "a smaller matrix of the same recipe (profiles/)"}
+    for h in hs.values():
+        h.destroy()
+    del coo
+    res["large"] = large
+    log(f"large done in {time.perf_counter() - t0:.1f} s")
+    # skewed power-law CSR: 500,000 x 500,000, ~50M nonzeros, width 64
+    t0 = time.perf_counter()
+    coo = W.make("skewed", seed=0, device=dev)
+    hs = build_handles(vs, coo, [("csr", "row")])
+    lb = layout_bytes_of(hs, coo)
+    specs = [("CSR@B", "csr", "row", "A@B", "deterministic"),
+             ("B@CSR", "csr", "row", "B@A", "deterministic"),
+             ("B@CSR", "csr", "row", "B@A", "atomic")]
+    sk = time_product_set(vs, torch, coo, hs, specs, 64, torch.float32, reps, timed, lb)
+    sk["cusparse"] = cusparse_times(torch, coo, hs, 64, torch.float32, reps, timed, sk)
+    sk["nnz"] = coo.nnz
+    for h in hs.values():
+        h.destroy()
+    del coo
+    res["skewed"] = sk
+    log(f"skewed done in {time.perf_counter() - t0:.1f} s")
+    torch.cuda.empty_cache()
+    return res
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -429,23 +665,35 @@ def gpu_arm(args):
 
     # ---- in-run cuSPARSE reference: torch's CSR matmul on the index-sorted CSR
     # (CSR@B), and on the CSR of the exact transpose for B@CSR (Y^T = A^T B^T)
-    cusparse = {}
-    import warnings
-    warnings.filterwarnings("ignore", message="Sparse CSR tensor support is in beta")
+    ours = {f"{k}/deterministic": {"ms": v} for k, v in ms_prod.items()}
+    cusparse = cusparse_times(torch, coo, handles, WIDTH, torch.float32, max(5, args.steps),
+                              timed, ours)
+
+    # ---- bit repeatability: 100 repeats of the same product, and each of three
+    # columns computed alone against the batch (cuSPARSE, then ours)
+    determinism = {}
     try:
+        import warnings
+        warnings.filterwarnings("ignore", message="Sparse CSR tensor support is in beta")
         a = handles[("csr", "row")].arrays()
         A_csr = torch.sparse_csr_tensor(a["ptr"], a["indices"], a["values"], (n_rows, n_cols))
-        with vs.build_csr(coo.cols, coo.rows, coo.vals, (n_cols, n_rows), "row") as hT:
-            t = hT.arrays()
-        AT_csr = torch.sparse_csr_tensor(t["ptr"], t["indices"], t["values"], (n_cols, n_rows))
-        for name, Am, X in (("CSR@B", A_csr, Bab), ("B@CSR", AT_csr, Bt)):
-            torch.mm(Am, X)
-            ts = timed(lambda: torch.mm(Am, X), max(5, args.steps))
-            ms = statistics.mean(ts)
-            cusparse[name] = {"ms": round(ms, 5), "GBs": round(nbytes[name] / ms / 1e6, 1),
-                              "ours_over_cusparse_time": round(ms_prod[name] / ms, 3)}
-    except Exception as exc:  # reported, never fatal: it is a comparison, not the path
-        cusparse = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
+        cols = (0, WIDTH // 2, WIDTH - 1)
+        determinism["cusparse CSR@B"] = bit_repeatability(
+            torch, lambda: torch.mm(A_csr, Bab), 100,
+            lambda c: torch.mm(A_csr, Bab[:, c:c + 1].contiguous()), cols)
+        for name, layout, major, direction in PRODUCTS:
+            A = handles[(layout, major)]
+            if direction == "A@B":
+                f = lambda A=A: vs.spmm(A, Bab, "A@B")
+                fc = lambda c, A=A: vs.spmm(A, Bab[:, c:c + 1].contiguous(), "A@B")
+            else:
+                f = lambda A=A: vs.spmm(A, Bt.t(), "B@A").t()
+                fc = lambda c, A=A: vs.spmm(A, Bt.t()[c:c + 1, :].t().contiguous().t(),
+                                            "B@A").t()
+            determinism[name] = bit_repeatability(torch, f, 100, fc, cols)
+        del A_csr
+    except Exception as exc:  # reported, never fatal
+        determinism = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
 
     # ---- the same products with L2 warm (no flush between reps): labelled
     # context, not the metric; near-equal times say the kernels are bound on
@@ -508,6 +756,27 @@ def gpu_arm(args):
     e2e_s = statistics.mean(e2e_times)
     e2e_value = step_bytes * ws / e2e_s / 1e9
 
+    # ---- aggregate of the six products with no transpose attached: the aligned
+    # gathers plus the two-phase scheme for the misaligned products
+    nt_ms, nt_bytes = 0.0, 0
+    for name, layout, major, direction in PRODUCTS:
+        aligned = (direction == "A@B") == (major == "row")
+        if aligned:
+            nt_ms += ms_prod[name]
+            nt_bytes += nbytes[name]
+        else:
+            nt_ms += variants[f"{name}/two_phase"]["ms"]
+            nt_bytes += product_bytes(layout, major, direction, "two_phase")
+    no_transpose = {"ms_per_step": round(nt_ms, 5), "GBs": round(nt_bytes / nt_ms / 1e6, 1),
+                    "note": "aligned gathers + two-phase misaligned products (no transpose kept)"}
+
+    # ---- the regridding-shaped, large and skewed workloads (reported beside
+    # the headline; not part of its step)
+    extra = None
+    if not args.skip_extra and rank == 0:
+        extra = extra_workloads(vs, torch, dev, timed, max(5, min(args.steps, 10)),
+                                lambda m: print(m, file=sys.stderr, flush=True))
+
     # ---- roofline of the dominant kernel
     peak, peak_kind = _peaks()
     dom = max(ms_prod, key=ms_prod.get)
@@ -540,13 +809,8 @@ def gpu_arm(args):
     # ---- CPU baseline: the float64 oracle on host cores (rank 0, N=1 only)
     cpu = None
     if rank == 0 and ws == 1 and not args.skip_cpu:
-        coo_h = coo.to("cpu")
-        reps, secs = run_oracle_sample(oracle_prepare(coo_h), coo_h, Bab.double().cpu().numpy(),
-                                       Bt.double().cpu().numpy(), args.cpu_seconds)
-        cpu = {"value": round(step_bytes * reps / secs / 1e9, 4), "unit": "GB/s", "cores": 1,
-               "kind": "oracle",
-               "sample": f"the six float64 oracle products on the full workload, {reps} pass(es), "
-                         f"{secs:.1f} s"}
+        cpu = cpu_baseline_leg(coo.to("cpu"), Bab.double().cpu().numpy(),
+                               Bt.double().cpu().numpy(), step_bytes, args.cpu_seconds)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
@@ -577,6 +841,9 @@ def gpu_arm(args):
         "products_l2_warm_ms": l2_warm,
         "gather_floor_ms": floor_ms,
         "cusparse": cusparse,
+        "bit_repeatability": determinism,
+        "no_transpose": no_transpose,
+        "extra_workloads": extra,
         "assembly_ms": assembly,
         "wall_s_timed_region": round(wall, 3),
     }
@@ -598,6 +865,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum seconds of oracle work for cpu_baseline")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the cpu_baseline leg")
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="omit the regridding-shaped, large and skewed workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

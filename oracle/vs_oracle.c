@@ -347,7 +347,8 @@ int or_view_triples(int64_t nnz, const int32_t *ti, const int32_t *tj, const dou
 /* Both row-major with row stride w.  D receives sum |a| |x| per element.    */
 /* Aligned: each output row is summed in entry order by one thread, exactly  */
 /* as the serial products above add it.  Misaligned: thread k of T takes the */
-/* slices [n_major k / T, n_major (k+1) / T) into a private Y_k; then        */
+/* consecutive slices whose first entry lies in [nnz k / T, nnz (k+1) / T)   */
+/* into a private Y_k (whole slices, balanced by entries); then              */
 /* Y = Y_0 + Y_1 + ... in thread order, so the result depends on T only.     */
 /* n_threads <= 0 means every thread OpenMP offers.  Returns OR_ERR_ALLOC    */
 /* when the private outputs cannot be allocated.                             */
@@ -361,6 +362,28 @@ int or_threads_available(void)
 #endif
 }
 
+/* First entry of slice s, and the entry count. */
+static int64_t slice_entry(const int32_t *ptr, const int32_t *vptr, int64_t s)
+{
+    return vptr ? vptr[ptr[s]] : ptr[s];
+}
+
+static int64_t nnz_of(int64_t n_major, const int32_t *ptr, const int32_t *vptr)
+{
+    return slice_entry(ptr, vptr, n_major);
+}
+
+/* The first slice s whose first entry is >= e (n_major if none). */
+static int64_t first_slice_at(int64_t n_major, const int32_t *ptr, const int32_t *vptr, int64_t e)
+{
+    int64_t lo = 0, hi = n_major;
+    while (lo < hi) {
+        int64_t mid = lo + (hi - lo) / 2;
+        if (slice_entry(ptr, vptr, mid) < e) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
 int or_spmm_slices(int64_t n_major, int64_t n_minor, const int32_t *ptr, const int32_t *vptr,
                    const int32_t *idx, const double *vals, int aligned, const double *X,
                    int64_t w, double *Y, double *D, int n_threads)
@@ -370,7 +393,7 @@ int or_spmm_slices(int64_t n_major, int64_t n_minor, const int32_t *ptr, const i
     if (T < 1) T = 1;
     if (aligned) {
 #ifdef _OPENMP
-#pragma omp parallel for schedule(static) num_threads(T)
+#pragma omp parallel for schedule(dynamic, 64) num_threads(T)
 #endif
         for (int64_t s = 0; s < n_major; s++) {
             double *y = Y + s * w, *d = D + s * w;
@@ -400,7 +423,9 @@ int or_spmm_slices(int64_t n_major, int64_t n_minor, const int32_t *ptr, const i
 #endif
     for (int k = 0; k < T; k++) {
         double *y = priv + (size_t)k * per * 2, *d = y + per;
-        int64_t s0 = n_major * k / T, s1 = n_major * (k + 1) / T;
+        int64_t s0 = first_slice_at(n_major, ptr, vptr, nnz_of(n_major, ptr, vptr) * k / T);
+        int64_t s1 = first_slice_at(n_major, ptr, vptr, nnz_of(n_major, ptr, vptr) * (k + 1) / T);
+        if (k == T - 1) s1 = n_major;
         for (int64_t s = s0; s < s1; s++) {
             const double *x = X + s * w;
             for (int64_t q = ptr[s]; q < ptr[s + 1]; q++) {

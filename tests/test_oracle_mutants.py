@@ -70,8 +70,8 @@ MUTANTS = {
     "slices_value_by_entry": ("                for (int64_t k = k0; k < k1; k++) {\n                    const double *x = X + (int64_t)idx[k] * w;",
                               "                for (int64_t k = k0; k < k1; k++) {\n                    a = vals[k < hi ? k : q];\n                    const double *x = X + (int64_t)idx[k] * w;"),
     # or_spmm_slices: each thread's slice range ends one slice early
-    "slices_range_short": ("        int64_t s0 = n_major * k / T, s1 = n_major * (k + 1) / T;",
-                           "        int64_t s0 = n_major * k / T, s1 = n_major * (k + 1) / T - (n_major * (k + 1) / T > n_major * k / T);"),
+    "slices_range_short": ("        if (k == T - 1) s1 = n_major;",
+                           "        if (k == T - 1) s1 = n_major;\n        if (s1 > s0) s1 -= 1;"),
 }
 
 
