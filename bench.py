@@ -371,10 +371,8 @@ def time_product_set(vs, torch, coo, handles, specs, width: int, dtype, reps: in
         A = handles[(layout, major)]
         B = Bab if direction == "A@B" else Bt.t()
         o = vs.empty_out(A, width, direction, dtype=dtype)
-        aligned = (direction == "A@B") == (major == "row")
-        m = major if aligned or variant not in ("deterministic", "transposed") else \
-            ("col" if major == "row" else "row")
-        nb = int(layout_bytes[(layout, m)] + (coo.n_rows + coo.n_cols) * width * es)
+        # the named product's own layout (the algorithmic bytes), whatever route runs it
+        nb = int(layout_bytes[(layout, major)] + (coo.n_rows + coo.n_cols) * width * es)
         vs.spmm(A, B, direction, variant, out=o)
         ts = timed(lambda: vs.spmm(A, B, direction, variant, out=o), reps)
         ms = statistics.median(ts)
@@ -387,7 +385,7 @@ def time_product_set(vs, torch, coo, handles, specs, width: int, dtype, reps: in
 
 
 def cusparse_times(torch, coo_dev, handles, width: int, dtype, reps: int, timed, ours: dict,
-                   seed: int = 1):
+                   seed: int = 1, names=None):
     """torch's CSR matmul (cuSPARSE SpMM) on the index-sorted CSR (CSR@B) and on
     the CSR of the exact transpose (B@CSR), beside our deterministic times."""
     import warnings
@@ -414,8 +412,9 @@ def cusparse_times(torch, coo_dev, handles, width: int, dtype, reps: int, timed,
             torch.mm(Am, X)
             ms = statistics.median(timed(lambda: torch.mm(Am, X), reps))
             entry = {"ms": round(ms, 5)}
-            key = f"{name}/deterministic"
+            key = f"{(names or {}).get(name, name)}/deterministic"
             if key in ours:
+                entry["ours"] = key
                 entry["ours_over_cusparse_time"] = round(ours[key]["ms"] / ms, 3)
             res[name] = entry
         del A_csr, AT_csr, Bab, Bt
@@ -487,7 +486,9 @@ def extra_workloads(vs, torch, dev, timed, reps: int, log):
                  ("B@VCSR", "vcs", "row", "B@A", "atomic"),
                  ("B@VCSC", "vcs", "col", "B@A", "deterministic")]
         times = time_product_set(vs, torch, coo, hs, specs, w, torch.float32, reps, timed, lb)
-        times["cusparse"] = cusparse_times(torch, coo, hs, w, torch.float32, reps, timed, {})
+        # cuSPARSE on the index-sorted CSR of the same matrix, beside VCSR@B and B@VCSC
+        times["cusparse"] = cusparse_times(torch, coo, hs, w, torch.float32, reps, timed, times,
+                                           names={"CSR@B": "VCSR@B", "B@CSR": "B@VCSC"})
         large[f"w{w}"] = times
     det = {k: v for k, v in large["w32"].items() if k.endswith("/deterministic")}
     dom = max(det, key=lambda k: det[k]["ms"])
@@ -579,9 +580,13 @@ def gpu_arm(args):
                    ("vcs", "col"): handles[("vcs", "col")].nbytes()[0],
                    ("csr", "row"): csr_bytes, ("csr", "col"): csc_bytes}
 
-    def product_bytes(layout, major, direction, variant="deterministic"):
+    def product_bytes(layout, major, direction, variant="deterministic", streamed=False):
+        """Algorithmic bytes of the named product: its own stored layout, B read
+        once, out written once.  streamed=True counts instead the layout the
+        kernel walks (the other-major transpose for a misaligned product run
+        over it)."""
         aligned = (direction == "A@B") == (major == "row")
-        if not aligned and variant in ("deterministic", "transposed"):
+        if streamed and not aligned and variant in ("deterministic", "transposed"):
             major = "col" if major == "row" else "row"
         nx = n_cols if direction == "A@B" else n_rows
         ny = n_rows if direction == "A@B" else n_cols
@@ -589,6 +594,8 @@ def gpu_arm(args):
 
     nbytes = {name: product_bytes(layout, major, direction)
               for name, layout, major, direction in PRODUCTS}
+    nbytes_streamed = {name: product_bytes(layout, major, direction, streamed=True)
+                       for name, layout, major, direction in PRODUCTS}
 
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     flush_sum = torch.empty((), dtype=torch.float32, device=dev)
@@ -785,7 +792,7 @@ def gpu_arm(args):
                     "GBs": round(nbytes[k] / ms_prod[k] / 1e6, 1),
                     "frac_of_8TBs": round(nbytes[k] / ms_prod[k] / 1e6 / NOMINAL_HBM_GBS, 4),
                     "frac_of_measured": round(nbytes[k] / ms_prod[k] / 1e6 / peak, 4),
-                    "bytes": nbytes[k]} for k in ms_prod}
+                    "bytes": nbytes[k], "bytes_streamed": nbytes_streamed[k]} for k in ms_prod}
     traffic = recorded_traffic(dom)
     # the second roof: every stored entry brings a row of w values of X through
     # L1 or shared memory, at most 128 bytes per clock per SM (nominal width)
