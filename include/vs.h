@@ -30,7 +30,10 @@
  *  - Errors are returned as vs_status; nothing is thrown across the ABI.
  *    vs_last_error() gives a message for the calling thread's last failure.
  *    On error, output buffers are left in an unspecified state.
- *  - Index arrays are int32; nnz must be below 2^31.
+ *  - Indices (minor coordinates) are int32, so rows and columns stay below
+ *    2^31.  Slice pointers are int32 when nnz < 2^31, and int64 ("Regridder",
+ *    "Why not cuSPARSE": 64-bit row pointers with 32-bit indices) for larger
+ *    matrices or when vs_build_options asks for them.
  *  - Dense operands are described by vs_dense (logical rows x cols plus
  *    strides in elements).  The width axis of B and out must have stride 1:
  *    for A@B that is the column axis (row-major B and out); for B@A it is the
@@ -118,16 +121,44 @@ typedef struct {
     int64_t n_chunks;       /* chunks over all long slices */
     int64_t n_blocks;       /* blocks the kernels stream (runs of short slices, or chunks) */
     int32_t has_transpose;  /* 1 once vs_attach_transpose succeeded */
+    int32_t pointer_bits;   /* 32 or 64: the width of the stored slice pointers */
+    int32_t n_segments;     /* kernel segments (64-bit pointers: consecutive slice ranges of
+                               fewer than 2^31 entries each; 1 otherwise) */
     int32_t reserved;
 } vs_info_t;
 
 typedef struct {
-    const int32_t *ptr;       /* n_major+1: CSR slice starts, or VCS major_ptr (run starts) */
+    const void *ptr;          /* n_major+1: CSR slice starts, or VCS major_ptr (run starts);
+                                 int32, or int64 when pointer_bits is 64 */
     const int32_t *indices;   /* nnz minor indices */
     const void *values;       /* CSR: nnz values of the handle dtype; VCS: R float32 run values */
-    const int32_t *value_ptr; /* VCS: R+1 index starts of the runs; CSR: NULL */
+    const void *value_ptr;    /* VCS: R+1 index starts of the runs, int32 or int64 like ptr;
+                                 CSR: NULL */
     int64_t n_major, nnz, n_runs;
+    int32_t pointer_bits;     /* 32 or 64 */
+    int32_t reserved;
 } vs_arrays;
+
+/*
+ * Build options (vs_build_csr_opts, vs_build_vcs_opts).
+ *   pointer_bits     0: automatic -- int32 slice pointers below 2^31 entries,
+ *                    int64 from 2^31 on; 32 or 64 to choose (32 with 2^31 or
+ *                    more entries is VS_ERR_UNSUPPORTED).  With int64 pointers
+ *                    the stored layout is ptr (and VCS value_ptr) of int64 with
+ *                    int32 indices; the products run the same kernels over
+ *                    consecutive slice ranges ("segments") of fewer than 2^31
+ *                    entries, and give the same bits as an int32 build.
+ *   segment_entries  0: the largest segment the int32 kernels take (about
+ *                    2^31 entries); otherwise at most this many entries per
+ *                    segment (a slice with more is a segment of its own) --
+ *                    lets a small matrix run the many-segment path, as one of
+ *                    more than 2^31 entries does.
+ */
+typedef struct {
+    int32_t pointer_bits;
+    int32_t reserved;
+    int64_t segment_entries;
+} vs_build_options;
 
 /*
  * vs_build_csr -- CSR (major = VS_MAJOR_ROW) or CSC (VS_MAJOR_COL) of COO
@@ -138,7 +169,8 @@ typedef struct {
  * bit for bit.
  *
  *   n_rows, n_cols   matrix shape (>= 0, < 2^31)
- *   nnz              number of triples (>= 0, < 2^31)
+ *   nnz              number of triples (>= 0; from 2^31 on the slice pointers
+ *                    are int64, see vs_build_options)
  *   d_row, d_col     device int32[nnz] coordinates
  *   d_val            device values[nnz] of `dtype` (float32 or float64)
  *   major            VS_MAJOR_ROW for CSR, VS_MAJOR_COL for CSC
@@ -151,6 +183,25 @@ typedef struct {
 vs_status vs_build_csr(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
                        const int32_t *d_col, const void *d_val, vs_dtype dtype, vs_major major,
                        cudaStream_t stream, vs_handle *out);
+
+/*
+ * vs_build_csr_opts, vs_build_vcs_opts -- vs_build_csr and vs_build_vcs with
+ * build options (NULL: the defaults, as vs_build_csr / vs_build_vcs).  nnz may
+ * reach 2^31 and beyond with 64-bit slice pointers; rows and columns stay
+ * below 2^31.  The assembly is the same counting sort: the range and NaN checks
+ * and the per-slice counts run over all entries, then each segment's entries
+ * are selected in input order and placed like an int32 build's, so the
+ * arrays are those of one stable sort.  Errors as for vs_build_csr /
+ * vs_build_vcs; VS_ERR_INVALID for bad options, VS_ERR_UNSUPPORTED when one
+ * slice holds 2^31 entries or more.
+ */
+vs_status vs_build_csr_opts(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
+                            const int32_t *d_col, const void *d_val, vs_dtype dtype,
+                            vs_major major, const vs_build_options *opts, cudaStream_t stream,
+                            vs_handle *out);
+vs_status vs_build_vcs_opts(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
+                            const int32_t *d_col, const float *d_val, vs_major major,
+                            const vs_build_options *opts, cudaStream_t stream, vs_handle *out);
 
 /*
  * vs_build_vcs -- VCSR (major = VS_MAJOR_ROW) or VCSC (VS_MAJOR_COL) of COO
@@ -229,7 +280,9 @@ vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direct
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array, which keeps whatever the last call
  * left in it; calls whose work overlaps on the GPU (other streams, other
- * threads) race on it and must be serialised by the caller.  The looked-up
+ * threads) race on it and must be serialised by the caller.  For a matrix
+ * with 64-bit slice pointers a misaligned product needs the transposed route
+ * (VS_ERR_UNSUPPORTED otherwise).  The looked-up
  * address is kept for the life of the process, so resetting a device
  * (cudaDeviceReset) while the library is loaded is not supported.
  */

@@ -41,7 +41,14 @@ class Info(ctypes.Structure):
                 ("chunk_len", ctypes.c_int64), ("n_long_slices", ctypes.c_int64),
                 ("n_chunks", ctypes.c_int64), ("n_blocks", ctypes.c_int64),
                 ("has_transpose", ctypes.c_int32),
+                ("pointer_bits", ctypes.c_int32),
+                ("n_segments", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
+
+
+class BuildOptions(ctypes.Structure):
+    _fields_ = [("pointer_bits", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("segment_entries", ctypes.c_int64)]
 
 
 class View(ctypes.Structure):
@@ -55,7 +62,8 @@ MAPS = {"identity": 0, "log1p": 1, "sqrt": 2}
 class Arrays(ctypes.Structure):
     _fields_ = [("ptr", ctypes.c_void_p), ("indices", ctypes.c_void_p), ("values", ctypes.c_void_p),
                 ("value_ptr", ctypes.c_void_p), ("n_major", ctypes.c_int64), ("nnz", ctypes.c_int64),
-                ("n_runs", ctypes.c_int64)]
+                ("n_runs", ctypes.c_int64), ("pointer_bits", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class VsError(RuntimeError):
@@ -81,6 +89,10 @@ def load() -> ctypes.CDLL:
         H = ctypes.c_void_p
         lib.vs_build_csr.argtypes = [i64, i64, i64, vp, vp, vp, i32, i32, vp, ctypes.POINTER(H)]
         lib.vs_build_vcs.argtypes = [i64, i64, i64, vp, vp, vp, i32, vp, ctypes.POINTER(H)]
+        lib.vs_build_csr_opts.argtypes = [i64, i64, i64, vp, vp, vp, i32, i32,
+                                          ctypes.POINTER(BuildOptions), vp, ctypes.POINTER(H)]
+        lib.vs_build_vcs_opts.argtypes = [i64, i64, i64, vp, vp, vp, i32,
+                                          ctypes.POINTER(BuildOptions), vp, ctypes.POINTER(H)]
         lib.vs_spmm.argtypes = [H, ctypes.POINTER(Dense), ctypes.POINTER(Dense), i32, i32, vp]
         lib.vs_spmm_host.argtypes = [H, ctypes.POINTER(Dense), ctypes.POINTER(Dense), i32, i32, vp]
         lib.vs_spmm_noalloc.argtypes = [H, ctypes.POINTER(Dense), ctypes.POINTER(Dense), i32, vp]
@@ -98,7 +110,7 @@ def load() -> ctypes.CDLL:
         lib.vs_export.argtypes = [H, ctypes.POINTER(Arrays)]
         lib.vs_handle_bytes.argtypes = [H, ctypes.POINTER(i64), ctypes.POINTER(i64)]
         lib.vs_destroy.argtypes = [H]
-        for f in ("vs_build_csr", "vs_build_vcs", "vs_spmm", "vs_spmm_host", "vs_spmm_noalloc",
+        for f in ("vs_build_csr", "vs_build_vcs", "vs_build_csr_opts", "vs_build_vcs_opts", "vs_spmm", "vs_spmm_host", "vs_spmm_noalloc",
                   "vs_spmm_view",
                   "vs_attach_transpose", "vs_transpose", "vs_scale_entries", "vs_force_group_size", "vs_gather_floor", "vs_device_status",
                   "vs_info", "vs_export", "vs_handle_bytes", "vs_destroy"):

@@ -82,11 +82,12 @@ class SparseMatrix:
             cai = _DeviceArray(ptr, n, _TYPESTR[dtype])
             return torch.as_tensor(cai, device=self.device).clone()
 
-        res = {"ptr": view(a.ptr, n_major + 1, torch.int32),
+        pt = torch.int64 if a.pointer_bits == 64 else torch.int32
+        res = {"ptr": view(a.ptr, n_major + 1, pt),
                "indices": view(a.indices, nnz, torch.int32)}
         if vcs:
             res["values"] = view(a.values, R, torch.float32)
-            res["value_ptr"] = view(a.value_ptr, R + 1, torch.int32)
+            res["value_ptr"] = view(a.value_ptr, R + 1, pt)
         else:
             res["values"] = view(a.values, nnz, self.dtype)
         return res
@@ -147,7 +148,7 @@ class SparseMatrix:
         self.destroy()
 
 
-_TYPESTR = {torch.int32: "<i4", torch.float32: "<f4", torch.float64: "<f8"}
+_TYPESTR = {torch.int32: "<i4", torch.int64: "<i8", torch.float32: "<f4", torch.float64: "<f8"}
 
 
 class _DeviceArray:
@@ -167,33 +168,54 @@ def _coo_args(rows: torch.Tensor, cols: torch.Tensor, vals: torch.Tensor):
     return rows.contiguous(), cols.contiguous(), vals.contiguous()
 
 
+def _options(pointer_bits, segment_entries):
+    if pointer_bits is None and segment_entries is None:
+        return None
+    return L.BuildOptions(int(pointer_bits or 0), 0, int(segment_entries or 0))
+
+
 def build_csr(rows: torch.Tensor, cols: torch.Tensor, vals: torch.Tensor, shape,
-              major: str = "row") -> SparseMatrix:
-    """``vs_build_csr``: CSR (major="row") or CSC (major="col") from device COO.
+              major: str = "row", *, pointer_bits: int | None = None,
+              segment_entries: int | None = None) -> SparseMatrix:
+    """``vs_build_csr`` (``vs_build_csr_opts`` with options): CSR (major="row")
+    or CSC (major="col") from device COO.
 
     Each slice keeps its entries in COO input order ("Regridder", "How it is built").
+    ``pointer_bits`` (32, 64; default automatic) and ``segment_entries`` are
+    the build options of include/vs.h.
     """
     rows, cols, vals = _coo_args(rows, cols, vals)
     if vals.dtype not in _DTYPES:
         raise TypeError("values must be float32 or float64")
     h = ctypes.c_void_p()
-    L.check(L.load().vs_build_csr(int(shape[0]), int(shape[1]), rows.numel(), rows.data_ptr(),
-                                  cols.data_ptr(), vals.data_ptr(), _DTYPES[vals.dtype],
-                                  _MAJORS[major], ctypes.c_void_p(_stream_ptr(rows.device)),
-                                  ctypes.byref(h)))
+    opts = _options(pointer_bits, segment_entries)
+    args = (int(shape[0]), int(shape[1]), rows.numel(), rows.data_ptr(), cols.data_ptr(),
+            vals.data_ptr(), _DTYPES[vals.dtype], _MAJORS[major])
+    stream = ctypes.c_void_p(_stream_ptr(rows.device))
+    if opts is None:
+        L.check(L.load().vs_build_csr(*args, stream, ctypes.byref(h)))
+    else:
+        L.check(L.load().vs_build_csr_opts(*args, ctypes.byref(opts), stream, ctypes.byref(h)))
     return SparseMatrix(h.value, shape, rows.device)
 
 
 def build_vcs(rows: torch.Tensor, cols: torch.Tensor, vals: torch.Tensor, shape,
-              major: str = "row") -> SparseMatrix:
-    """``vs_build_vcs``: VCSR (major="row") or VCSC (major="col") from device COO (float32)."""
+              major: str = "row", *, pointer_bits: int | None = None,
+              segment_entries: int | None = None) -> SparseMatrix:
+    """``vs_build_vcs`` (``vs_build_vcs_opts`` with options): VCSR (major="row")
+    or VCSC (major="col") from device COO (float32)."""
     rows, cols, vals = _coo_args(rows, cols, vals)
     if vals.dtype != torch.float32:
         raise TypeError("VCS values are float32")
     h = ctypes.c_void_p()
-    L.check(L.load().vs_build_vcs(int(shape[0]), int(shape[1]), rows.numel(), rows.data_ptr(),
-                                  cols.data_ptr(), vals.data_ptr(), _MAJORS[major],
-                                  ctypes.c_void_p(_stream_ptr(rows.device)), ctypes.byref(h)))
+    opts = _options(pointer_bits, segment_entries)
+    args = (int(shape[0]), int(shape[1]), rows.numel(), rows.data_ptr(), cols.data_ptr(),
+            vals.data_ptr(), _MAJORS[major])
+    stream = ctypes.c_void_p(_stream_ptr(rows.device))
+    if opts is None:
+        L.check(L.load().vs_build_vcs(*args, stream, ctypes.byref(h)))
+    else:
+        L.check(L.load().vs_build_vcs_opts(*args, ctypes.byref(opts), stream, ctypes.byref(h)))
     return SparseMatrix(h.value, shape, rows.device)
 
 

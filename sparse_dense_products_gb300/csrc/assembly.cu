@@ -508,27 +508,349 @@ vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dty
   return VS_OK;
 }
 
+// ------------------------------------------------------------------ wide matrices
+
+namespace {
+
+// flags[0]: a coordinate outside the matrix; flags[1]: a NaN value (VCS keys)
+__global__ void wide_check_kernel(const int32_t *__restrict__ maj, const int32_t *__restrict__ mnr,
+                                  const float *__restrict__ val, int64_t nnz, int64_t n_major,
+                                  int64_t n_minor, int *flags) {
+  int range = 0, nan = 0;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < nnz;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int a = maj[t], b = mnr[t];
+    if (a < 0 || a >= n_major || b < 0 || b >= n_minor) range = 1;
+    if (val && (__float_as_uint(val[t]) & 0x7fffffffu) > 0x7f800000u) nan = 1;
+  }
+  range = __syncthreads_or(range);
+  nan = __syncthreads_or(nan);
+  if (threadIdx.x == 0) {
+    if (range) atomicOr(&flags[0], 1);
+    if (nan) atomicOr(&flags[1], 1);
+  }
+}
+
+__global__ void count64_kernel(const int32_t *__restrict__ maj, int64_t n,
+                               unsigned long long *__restrict__ cnt) {
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n;
+       t += (int64_t)gridDim.x * blockDim.x)
+    atomicAdd(&cnt[maj[t]], 1ull);
+}
+
+// Selection of the entries whose major index lies in [s0, s1), in input
+// order: tile b (kTile entries) counts its matches, an exclusive scan of the
+// counts gives each tile's first output position, and the tile writes its
+// matches in order (thread k holds entries k*kItems .. k*kItems+kItems-1 of
+// the tile; a block scan orders the threads).
+__global__ void select_count_kernel(const int32_t *__restrict__ maj, int64_t n, int s0, int s1,
+                                    int64_t *__restrict__ tile_count) {
+  const int64_t base = (int64_t)blockIdx.x * kTile + (int64_t)threadIdx.x * kItems;
+  int c = 0;
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const int64_t i = base + k;
+    if (i < n && maj[i] >= s0 && maj[i] < s1) ++c;
+  }
+  int total;
+  block_exclusive_scan<kThreads>(c, total);
+  if (threadIdx.x == 0) tile_count[blockIdx.x] = total;
+}
+
+__global__ void select_write_kernel(const int32_t *__restrict__ maj, const int32_t *__restrict__ mnr,
+                                    const uint32_t *__restrict__ val, int words, int64_t n, int s0,
+                                    int s1, const int64_t *__restrict__ tile_first,
+                                    int32_t *__restrict__ out_maj, int32_t *__restrict__ out_mnr,
+                                    uint32_t *__restrict__ out_val) {
+  const int64_t base = (int64_t)blockIdx.x * kTile + (int64_t)threadIdx.x * kItems;
+  bool keep[kItems];
+  int c = 0;
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const int64_t i = base + k;
+    keep[k] = i < n && maj[i] >= s0 && maj[i] < s1;
+    c += keep[k];
+  }
+  int total;
+  int64_t pos = tile_first[blockIdx.x] + block_exclusive_scan<kThreads>(c, total);
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    if (!keep[k]) continue;
+    const int64_t i = base + k;
+    out_maj[pos] = maj[i] - s0;
+    out_mnr[pos] = mnr[i];
+    for (int q = 0; q < words; ++q) out_val[pos * words + q] = val[i * words + q];
+    ++pos;
+  }
+}
+
+// p[i] += d, i < n
+__global__ void shift_kernel(int32_t *__restrict__ p, int64_t n, int32_t d) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    p[i] += d;
+}
+
+// out[i] = d for i < lead; out[lead + i] = d + src[i] for i < n
+__global__ void lead_shift_kernel(const int32_t *__restrict__ src, int64_t n, int lead, int32_t d,
+                                  int32_t *__restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n + lead;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = i < lead ? d : d + src[i - lead];
+}
+
+// dst[i] = add + src[i], i < n
+__global__ void widen_kernel(const int32_t *__restrict__ src, int64_t n, int64_t add,
+                             int64_t *__restrict__ dst) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = add + (int64_t)src[i];
+}
+
+}  // namespace
+
+vs_status build_wide(Matrix &m, vs_layout layout, vs_major major, vs_dtype dtype, int64_t n_rows,
+                     int64_t n_cols, int64_t nnz, const int32_t *d_row, const int32_t *d_col,
+                     const void *d_val, int64_t seg_entries, cudaStream_t s) {
+  m.layout = layout;
+  m.major = major;
+  m.dtype = dtype;
+  m.n_rows = n_rows;
+  m.n_cols = n_cols;
+  m.n_major = major == VS_MAJOR_ROW ? n_rows : n_cols;
+  m.n_minor = major == VS_MAJOR_ROW ? n_cols : n_rows;
+  m.nnz = nnz;
+  m.wide = true;
+  m.seg_entries = seg_entries > 0 ? std::min(seg_entries, kMaxSegmentEntries) : kMaxSegmentEntries;
+  const int32_t *maj = major == VS_MAJOR_ROW ? d_row : d_col;
+  const int32_t *mnr = major == VS_MAJOR_ROW ? d_col : d_row;
+  const bool vcs = layout == VS_LAYOUT_VCS;
+  const size_t dsize = m.dsize();
+  const unsigned eg = std::min<unsigned>(kGridCap, grid_for(nnz, 256));
+
+  // ---- checks over every entry, and the entries of each slice
+  Temp flags(s), cnt(s);
+  VS_TRY(flags.alloc(2 * sizeof(int)));
+  VS_CUDA(cudaMemsetAsync(flags.p, 0, 2 * sizeof(int), s));
+  VS_TRY(cnt.alloc(sizeof(unsigned long long) * (size_t)std::max<int64_t>(m.n_major, 1)));
+  VS_CUDA(cudaMemsetAsync(cnt.p, 0, sizeof(unsigned long long) * (size_t)std::max<int64_t>(m.n_major, 1), s));
+  int hflags[2] = {0, 0};
+  if (nnz > 0) {
+    wide_check_kernel<<<eg, 256, 0, s>>>(maj, mnr, vcs ? static_cast<const float *>(d_val) : nullptr,
+                                         nnz, m.n_major, m.n_minor, flags.as<int>());
+    VS_LAUNCH_CHECK();
+    VS_CUDA(cudaMemcpyAsync(hflags, flags.p, sizeof hflags, cudaMemcpyDeviceToHost, s));
+    VS_CUDA(cudaStreamSynchronize(s));
+    if (hflags[0]) {
+      set_error("a COO coordinate lies outside the matrix");
+      return VS_ERR_RANGE;
+    }
+    if (hflags[1]) {
+      set_error("NaN value: VCS runs need an ordered value key");
+      return VS_ERR_NAN;
+    }
+    count64_kernel<<<eg, 256, 0, s>>>(maj, nnz, cnt.as<unsigned long long>());
+    VS_LAUNCH_CHECK();
+  }
+  std::vector<unsigned long long> counts((size_t)m.n_major);
+  if (m.n_major > 0)
+    VS_CUDA(cudaMemcpyAsync(counts.data(), cnt.p, sizeof(unsigned long long) * counts.size(),
+                            cudaMemcpyDeviceToHost, s));
+  VS_CUDA(cudaStreamSynchronize(s));
+  std::vector<int64_t> start((size_t)m.n_major + 1, 0);  // entry start of each slice
+  for (int64_t k = 0; k < m.n_major; ++k) {
+    if ((int64_t)counts[k] > kMaxSegmentEntries) {
+      set_error("a slice holds more entries than one kernel segment takes (about 2^31)");
+      return VS_ERR_UNSUPPORTED;
+    }
+    start[k + 1] = start[k] + (int64_t)counts[k];
+  }
+
+  // ---- segments: consecutive slices with at most seg_entries entries (a
+  // longer slice alone)
+  std::vector<std::pair<int64_t, int64_t>> cuts;  // [s0, s1)
+  for (int64_t s0 = 0; s0 < m.n_major;) {
+    int64_t s1 = std::upper_bound(start.begin() + s0 + 1, start.end(), start[s0] + m.seg_entries) -
+                 start.begin() - 1;
+    s1 = std::max(s1, s0 + 1);
+    cuts.emplace_back(s0, s1);
+    s0 = s1;
+  }
+  VS_TRY(dev_alloc((void **)&m.ptr64, sizeof(int64_t) * (size_t)(m.n_major + 1 + 16)));
+  VS_CUDA(cudaMemsetAsync(m.ptr64, 0, sizeof(int64_t) * (size_t)(m.n_major + 1 + 16), s));
+  VS_TRY(dev_alloc((void **)&m.idx, sizeof(int32_t) * (size_t)(nnz + 16)));
+  VS_CUDA(cudaMemsetAsync(m.idx, 0, sizeof(int32_t) * (size_t)(nnz + 16), s));
+  if (!vcs) {
+    VS_TRY(dev_alloc(&m.vals, dsize * (size_t)(nnz + 16)));
+    VS_CUDA(cudaMemsetAsync(m.vals, 0, dsize * (size_t)(nnz + 16), s));
+  }
+  m.segs.resize(cuts.size());
+  const int64_t ntiles = std::max<int64_t>(1, (nnz + kTile - 1) / kTile);
+  Temp tile_count(s), tile_first(s);
+  VS_TRY(tile_count.alloc(sizeof(int64_t) * (size_t)ntiles));
+  VS_TRY(tile_first.alloc(sizeof(int64_t) * (size_t)ntiles));
+  std::vector<int64_t> htc((size_t)ntiles);
+  const int words = (int)((vcs ? sizeof(float) : dsize) / 4);
+  int64_t r_base = 0;
+  for (size_t k = 0; k < cuts.size(); ++k) {
+    Matrix &g = m.segs[k];
+    const int64_t s0 = cuts[k].first, s1 = cuts[k].second;
+    const int64_t e0 = start[s0], ne = start[s1] - start[s0];
+    // this segment's entries, in input order, with slice indices relative to s0
+    Temp smaj(s), smnr(s), sval(s);
+    VS_TRY(smaj.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(ne, 1)));
+    VS_TRY(smnr.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(ne, 1)));
+    VS_TRY(sval.alloc(sizeof(uint32_t) * words * (size_t)std::max<int64_t>(ne, 1)));
+    if (nnz > 0) {
+      select_count_kernel<<<(unsigned)ntiles, kThreads, 0, s>>>(maj, nnz, (int)s0, (int)s1,
+                                                                tile_count.as<int64_t>());
+      VS_LAUNCH_CHECK();
+      VS_CUDA(cudaMemcpyAsync(htc.data(), tile_count.p, sizeof(int64_t) * htc.size(),
+                              cudaMemcpyDeviceToHost, s));
+      VS_CUDA(cudaStreamSynchronize(s));
+      int64_t run = 0;
+      for (auto &c : htc) {
+        const int64_t v = c;
+        c = run;
+        run += v;
+      }
+      if (run != ne) {
+        set_error("internal: segment selection count mismatch");
+        return VS_ERR_CUDA;
+      }
+      VS_CUDA(cudaMemcpyAsync(tile_first.p, htc.data(), sizeof(int64_t) * htc.size(),
+                              cudaMemcpyHostToDevice, s));
+      select_write_kernel<<<(unsigned)ntiles, kThreads, 0, s>>>(
+          maj, mnr, static_cast<const uint32_t *>(d_val), words, nnz, (int)s0, (int)s1,
+          tile_first.as<int64_t>(), smaj.as<int32_t>(), smnr.as<int32_t>(), sval.as<uint32_t>());
+      VS_LAUNCH_CHECK();
+    }
+    // assembled like any int32 matrix (rows = the segment's slices)
+    VS_TRY(build_matrix(g, layout, VS_MAJOR_ROW, dtype, s1 - s0, m.n_minor, ne, smaj.as<int32_t>(),
+                        smnr.as<int32_t>(), sval.p, s));
+    g.major = major;
+    g.n_rows = major == VS_MAJOR_ROW ? s1 - s0 : m.n_minor;
+    g.n_cols = major == VS_MAJOR_ROW ? m.n_minor : s1 - s0;
+    g.seg_slice0 = s0;
+    const int64_t r0 = vcs ? r_base : e0, R_seg = g.R;
+    // the whole matrix's indices (and CSR values) take the segment's; the
+    // segment keeps views of them
+    if (ne > 0) {
+      VS_CUDA(cudaMemcpyAsync(m.idx + e0, g.idx, sizeof(int32_t) * (size_t)ne,
+                              cudaMemcpyDeviceToDevice, s));
+      if (!vcs)
+        VS_CUDA(cudaMemcpyAsync(static_cast<char *>(m.vals) + (size_t)e0 * dsize, g.vals,
+                                dsize * (size_t)ne, cudaMemcpyDeviceToDevice, s));
+    }
+    // 64-bit slice pointers: entry starts (CSR) or run starts (VCS)
+    const unsigned pg = std::min<unsigned>(kGridCap, grid_for(s1 - s0 + 1, 256));
+    widen_kernel<<<pg, 256, 0, s>>>(g.ptr, s1 - s0 + 1, r0, m.ptr64 + s0);
+    VS_LAUNCH_CHECK();
+    // The segment's views start at the 16-byte boundary at or before its first
+    // entry (and run), as the bulk copies of its blocks need: its slice
+    // pointers count from there, past `lead` entries (runs) of the previous
+    // segment that none of its slices names.
+    const int lead_e = (int)(e0 & 3), lead_r = vcs ? (int)(r0 & 3) : lead_e;
+    g.seg_entry0 = e0 - lead_e;
+    g.seg_run0 = r0 - lead_r;
+    g.seg_lead_e = lead_e;
+    g.seg_lead_r = lead_r;
+    if (lead_r) {
+      shift_kernel<<<pg, 256, 0, s>>>(g.ptr, s1 - s0 + 1, lead_r);
+      VS_LAUNCH_CHECK();
+    }
+    if (vcs) {
+      // run starts: lead_r leading runs (never named), the rest shifted by lead_e
+      int32_t *vp = nullptr;
+      VS_TRY(dev_alloc((void **)&vp, sizeof(int32_t) * (size_t)(R_seg + lead_r + 1 + 16)));
+      VS_CUDA(cudaMemsetAsync(vp, 0, sizeof(int32_t) * (size_t)(R_seg + lead_r + 1 + 16), s));
+      lead_shift_kernel<<<std::min<unsigned>(kGridCap, grid_for(R_seg + 1 + lead_r, 256)), 256, 0,
+                          s>>>(g.vptr, R_seg + 1, lead_r, lead_e, vp);
+      VS_LAUNCH_CHECK();
+      VS_CUDA(cudaStreamSynchronize(s));
+      cudaFree(g.vptr);
+      g.vptr = vp;
+      g.R = R_seg + lead_r;
+    } else {
+      g.R = ne + lead_e;
+    }
+    g.nnz = ne + lead_e;
+    VS_CUDA(cudaStreamSynchronize(s));
+    cudaFree(g.idx);
+    g.idx = m.idx + g.seg_entry0;
+    if (!vcs) {
+      cudaFree(g.vals);
+      g.vals = static_cast<char *>(m.vals) + (size_t)g.seg_entry0 * dsize;
+    }
+    g.borrowed_entries = true;
+    r_base += R_seg;
+  }
+  m.R = vcs ? r_base : nnz;
+  if (vcs) {
+    // run values and 64-bit run starts of the whole matrix
+    VS_TRY(dev_alloc(&m.vals, sizeof(float) * (size_t)(m.R + 16)));
+    VS_CUDA(cudaMemsetAsync(m.vals, 0, sizeof(float) * (size_t)(m.R + 16), s));
+    VS_TRY(dev_alloc((void **)&m.vptr64, sizeof(int64_t) * (size_t)(m.R + 1 + 16)));
+    VS_CUDA(cudaMemsetAsync(m.vptr64, 0, sizeof(int64_t) * (size_t)(m.R + 1 + 16), s));
+    for (Matrix &g : m.segs) {
+      // the segment's own runs (after its lead): values and 64-bit run starts
+      const int64_t r0 = g.seg_run0 + g.seg_lead_r, R_seg = g.R - g.seg_lead_r;
+      if (R_seg > 0)
+        VS_CUDA(cudaMemcpyAsync(static_cast<float *>(m.vals) + r0, g.vals,
+                                sizeof(float) * (size_t)R_seg, cudaMemcpyDeviceToDevice, s));
+      widen_kernel<<<std::min<unsigned>(kGridCap, grid_for(R_seg + 1, 256)), 256, 0, s>>>(
+          g.vptr + (r0 - g.seg_run0), R_seg + 1, g.seg_entry0, m.vptr64 + r0);
+      VS_LAUNCH_CHECK();
+    }
+    VS_CUDA(cudaStreamSynchronize(s));
+    for (Matrix &g : m.segs) {
+      cudaFree(g.vals);
+      g.vals = static_cast<float *>(m.vals) + g.seg_run0;
+    }
+  }
+  // kernel parameters of every segment, with the whole matrix's group size
+  m.g = group_size_rule(m.nnz, m.n_major);
+  m.sorted_segments = true;
+  for (Matrix &g : m.segs) {
+    VS_TRY(prepare_matrix(g, s));
+    g.g = m.g;
+    m.n_sm = g.n_sm;
+    m.sorted_segments = m.sorted_segments && g.sorted_segments;
+    m.n_blocks += g.n_blocks;
+    m.n_long += g.n_long;
+    m.n_chunks += g.n_chunks;
+  }
+  if (m.segs.empty()) {
+    int dev = 0;
+    VS_CUDA(cudaGetDevice(&dev));
+    VS_CUDA(cudaDeviceGetAttribute(&m.n_sm, cudaDevAttrMultiProcessorCount, dev));
+  }
+  return VS_OK;
+}
+
 // ------------------------------------------------------------------ transpose
 
 namespace {
 
-// COO of a stored layout, in layout order: (major, minor, value bits).
+// COO of a stored layout, in layout order: (major, minor, value bits).  The
+// major index written is slice0 + s (a segment of a wide matrix passes its
+// first slice, and output pointers already offset to its first entry).
 __global__ void expand_csr_kernel(const int32_t *__restrict__ ptr, int64_t n_major,
-                                  int32_t *__restrict__ out_major) {
+                                  int32_t *__restrict__ out_major, int64_t slice0 = 0) {
   for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < n_major;
        s += (int64_t)gridDim.x * blockDim.x)
-    for (int32_t k = ptr[s]; k < ptr[s + 1]; ++k) out_major[k] = (int32_t)s;
+    for (int32_t k = ptr[s]; k < ptr[s + 1]; ++k) out_major[k] = (int32_t)(slice0 + s);
 }
 
 __global__ void expand_vcs_kernel(const int32_t *__restrict__ major_ptr,
                                   const int32_t *__restrict__ vptr, const float *__restrict__ values,
                                   int64_t n_major, int32_t *__restrict__ out_major,
-                                  float *__restrict__ out_val) {
+                                  float *__restrict__ out_val, int64_t slice0 = 0) {
   for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < n_major;
        s += (int64_t)gridDim.x * blockDim.x)
     for (int32_t r = major_ptr[s]; r < major_ptr[s + 1]; ++r)
       for (int32_t k = vptr[r]; k < vptr[r + 1]; ++k) {
-        out_major[k] = (int32_t)s;
+        out_major[k] = (int32_t)(slice0 + s);
         out_val[k] = values[r];
       }
 }
@@ -538,6 +860,29 @@ __global__ void expand_vcs_kernel(const int32_t *__restrict__ major_ptr,
 vs_status build_transpose(const Matrix &src, Matrix &dst, cudaStream_t s) {
   const int64_t nnz = src.nnz;
   Temp maj(s), vals(s);
+  if (src.wide) {
+    // the COO of every segment into the whole matrix's positions, then a wide build
+    VS_TRY(maj.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(nnz, 1)));
+    const bool vcs = src.layout == VS_LAYOUT_VCS;
+    if (vcs) VS_TRY(vals.alloc(sizeof(float) * (size_t)std::max<int64_t>(nnz, 1)));
+    for (const Matrix &g : src.segs) {
+      if (g.n_major == 0) continue;
+      const unsigned gg = std::min<unsigned>(kGridCap, grid_for(g.n_major, 256));
+      if (vcs)
+        expand_vcs_kernel<<<gg, 256, 0, s>>>(g.ptr, g.vptr, static_cast<const float *>(g.vals),
+                                             g.n_major, maj.as<int32_t>() + g.seg_entry0,
+                                             vals.as<float>() + g.seg_entry0, g.seg_slice0);
+      else
+        expand_csr_kernel<<<gg, 256, 0, s>>>(g.ptr, g.n_major, maj.as<int32_t>() + g.seg_entry0,
+                                             g.seg_slice0);
+      VS_LAUNCH_CHECK();
+    }
+    const vs_major other = src.major == VS_MAJOR_ROW ? VS_MAJOR_COL : VS_MAJOR_ROW;
+    const int32_t *rows = src.major == VS_MAJOR_ROW ? maj.as<int32_t>() : src.idx;
+    const int32_t *cols = src.major == VS_MAJOR_ROW ? src.idx : maj.as<int32_t>();
+    return build_wide(dst, src.layout, other, src.dtype, src.n_rows, src.n_cols, nnz, rows, cols,
+                      vcs ? vals.p : src.vals, src.seg_entries, s);
+  }
   VS_TRY(maj.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(nnz, 1)));
   const unsigned g = std::min<unsigned>(kGridCap, grid_for(src.n_major, 256));
   const void *val_ptr = src.vals;
@@ -583,6 +928,7 @@ __global__ void unsorted_kernel(const int32_t *__restrict__ idx, const uint8_t *
 }  // namespace
 
 vs_status prepare_matrix(Matrix &m, cudaStream_t s) {
+  if (m.wide) return VS_OK;  // build_wide prepared every segment
   // slice entry ranges on the host
   std::vector<int32_t> ptr(m.n_major + 1), vptr;
   VS_CUDA(cudaMemcpyAsync(ptr.data(), m.ptr, sizeof(int32_t) * (m.n_major + 1),

@@ -14,6 +14,18 @@ vs_status launch_gather_mix_csr(const Matrix &m, DenseView X, DenseView Y, int64
 
 vs_status launch_gather(const Matrix &m, DenseView X, DenseView Y, int64_t w, cudaStream_t s) {
   if (w <= 0 || m.n_major == 0) return VS_OK;
+  if (m.wide) {
+    // each segment gathers its own slices: output rows from its first slice on
+    const size_t es = Y.f64 ? 8 : 4;
+    for (const Matrix &g : m.segs) {
+      DenseView Yg = Y;
+      Yg.p = static_cast<char *>(Y.p) + (size_t)g.seg_slice0 * (size_t)Y.ld * es;
+      Yg.rows = g.n_major;
+      if (Y.scale) Yg.scale = static_cast<const char *>(Y.scale) + (size_t)g.seg_slice0 * es;
+      VS_TRY(launch_gather(g, X, Yg, w, s));
+    }
+    return VS_OK;
+  }
   if (m.layout == VS_LAYOUT_VCS)
     return X.f64 ? launch_gather_f64_vcs(m, X, Y, w, s) : launch_gather_f32_vcs(m, X, Y, w, s);
   if (m.dtype == VS_F64) return launch_gather_f64_csr(m, X, Y, w, s);

@@ -139,6 +139,18 @@ __global__ void __launch_bounds__(kPipeThreads) scatter_atomic_kernel(const Scat
 
 // ------------------------------------------------------------------ zero fill
 
+// Y[r, c] += T[r, c] (T contiguous with row stride w)
+template <typename T>
+__global__ void add_into_kernel(const T *__restrict__ src, int64_t rows, int64_t w,
+                                T *__restrict__ Y, int64_t ld) {
+  const int64_t total = rows * w;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / w, c = i - r * w;
+    Y[r * ld + c] = Y[r * ld + c] + src[i];
+  }
+}
+
 template <typename T>
 __global__ void zero_fill_kernel(T *__restrict__ Y, int64_t rows, int64_t w, int64_t ld) {
   const int64_t total = rows * w;
@@ -861,6 +873,11 @@ vs_status two_phase_static_typed(const Matrix &m, DenseView X, DenseView Y, int6
 vs_status launch_scatter_two_phase_static(const Matrix &m, DenseView X, DenseView Y, int64_t w,
                                           cudaStream_t s) {
   if (w <= 0 || Y.rows == 0) return VS_OK;
+  if (m.wide) {
+    set_error("vs_spmm_noalloc: a misaligned product of a matrix with 64-bit slice pointers needs "
+              "the transposed route (vs_attach_transpose)");
+    return VS_ERR_UNSUPPORTED;
+  }
   if (m.n_major == 0 || m.nnz == 0) return launch_zero_fill(Y, w, m.dsize(), s);
   if (m.layout == VS_LAYOUT_VCS) return two_phase_static_typed<float, true>(m, X, Y, w, s);
   if (m.dtype == VS_F64) return two_phase_static_typed<double, false>(m, X, Y, w, s);
@@ -886,11 +903,33 @@ vs_status launch_zero_fill(DenseView Y, int64_t w, size_t dsize, cudaStream_t s)
   return VS_OK;
 }
 
+// The rows X[slice0, ...) of a misaligned product's operand: the operand of a
+// wide matrix's segment.
+static DenseView segment_rows(DenseView X, const Matrix &g) {
+  DenseView Xg = X;
+  Xg.p = static_cast<char *>(X.p) + (size_t)g.seg_slice0 * (size_t)X.ld * (X.f64 ? 8 : 4);
+  Xg.rows = g.n_major;
+  return Xg;
+}
+
 vs_status launch_scatter_atomic(const Matrix &m, DenseView X, DenseView Y, int64_t w,
                                 cudaStream_t s) {
   if (w <= 0) return VS_OK;
   VS_TRY(launch_zero_fill(Y, w, m.dsize(), s));
   if (m.n_major == 0 || m.nnz == 0) return VS_OK;
+  if (m.wide) {  // every segment adds into the same zero-filled output
+    for (const Matrix &g : m.segs) {
+      if (g.nnz == 0) continue;
+      const DenseView Xg = segment_rows(X, g);
+      if (g.layout == VS_LAYOUT_VCS)
+        VS_TRY((atomic_typed<float, true>(g, Xg, Y, w, s)));
+      else if (g.dtype == VS_F64)
+        VS_TRY((atomic_typed<double, false>(g, Xg, Y, w, s)));
+      else
+        VS_TRY((atomic_typed<float, false>(g, Xg, Y, w, s)));
+    }
+    return VS_OK;
+  }
   if (m.layout == VS_LAYOUT_VCS) return atomic_typed<float, true>(m, X, Y, w, s);
   if (m.dtype == VS_F64) return atomic_typed<double, false>(m, X, Y, w, s);
   return atomic_typed<float, false>(m, X, Y, w, s);
@@ -900,6 +939,38 @@ vs_status launch_scatter_two_phase(vs_handle_s &h, const Matrix &m, DenseView X,
                                    int64_t w, cudaStream_t s) {
   if (w <= 0 || Y.rows == 0) return VS_OK;
   if (m.n_major == 0 || m.nnz == 0) return launch_zero_fill(Y, w, m.dsize(), s);
+  if (m.wide) {
+    // segment 0 writes the output; each later segment's deterministic sum is
+    // added to it in segment order (slice order, like the groups of one piece)
+    const size_t es = m.dsize();
+    bool first = true;
+    for (const Matrix &g : m.segs) {
+      if (g.nnz == 0) continue;
+      const DenseView Xg = segment_rows(X, g);
+      if (first) {
+        VS_TRY(launch_scatter_two_phase(h, g, Xg, Y, w, s));
+        first = false;
+        continue;
+      }
+      VS_TRY(h.wide_tmp.reserve(es * (size_t)(Y.rows * w + 16), s));
+      DenseView T = Y;
+      T.p = h.wide_tmp.p;
+      T.ld = w;
+      T.scale = nullptr;
+      VS_TRY(launch_scatter_two_phase(h, g, Xg, T, w, s));
+      const int64_t total = Y.rows * w;
+      const unsigned blocks = (unsigned)std::min<int64_t>((int64_t)m.n_sm * 8, (total + 255) / 256);
+      if (es == 8)
+        add_into_kernel<double><<<std::max(1u, blocks), 256, 0, s>>>(
+            static_cast<const double *>(T.p), Y.rows, w, static_cast<double *>(Y.p), Y.ld);
+      else
+        add_into_kernel<float><<<std::max(1u, blocks), 256, 0, s>>>(
+            static_cast<const float *>(T.p), Y.rows, w, static_cast<float *>(Y.p), Y.ld);
+      VS_LAUNCH_CHECK();
+    }
+    if (first) return launch_zero_fill(Y, w, es, s);
+    return VS_OK;
+  }
   if (m.layout == VS_LAYOUT_VCS) return two_phase_typed<float, true>(h, m, X, Y, w, s);
   if (m.dtype == VS_F64) return two_phase_typed<double, false>(h, m, X, Y, w, s);
   return two_phase_typed<float, false>(h, m, X, Y, w, s);

@@ -43,15 +43,24 @@ vs_status cuda_status(cudaError_t e, const char *what) {
 }
 
 int64_t Matrix::layout_bytes() const {
-  int64_t b = (int64_t)sizeof(int32_t) * (n_major + 1) + (int64_t)sizeof(int32_t) * nnz;
+  const int64_t pb = wide ? 8 : 4;  // bytes per slice pointer
+  int64_t b = pb * (n_major + 1) + (int64_t)sizeof(int32_t) * nnz;
   if (layout == VS_LAYOUT_VCS)
-    b += (int64_t)sizeof(float) * R + (int64_t)sizeof(int32_t) * (R + 1);
+    b += (int64_t)sizeof(float) * R + pb * (R + 1);
   else
     b += (int64_t)dsize() * nnz;
   return b;
 }
 
 int64_t Matrix::meta_bytes() const {
+  if (wide) {  // each segment's own slice pointers and kernel parameters
+    int64_t b = 0;
+    for (const Matrix &g : segs) {
+      b += (int64_t)sizeof(int32_t) * (g.n_major + 1) + g.meta_bytes();
+      if (g.layout == VS_LAYOUT_VCS) b += (int64_t)sizeof(int32_t) * (g.R + 1);
+    }
+    return b;
+  }
   return (int64_t)sizeof(int4) * 3 * n_blocks + (int64_t)sizeof(int4) * n_long + (int64_t)sizeof(int) +
          (int64_t)sizeof(double) * kMaxBlockWidth * n_shares + (int64_t)sizeof(int32_t) * (tp_chunks + 1);
 }
@@ -59,23 +68,41 @@ int64_t Matrix::meta_bytes() const {
 namespace {
 // The index arrays of a matrix, freed when the last matrix using them goes.
 struct IndexArrays {
-  void *p[6];
+  std::vector<void *> p;
   ~IndexArrays() {
     for (void *q : p)
       if (q) cudaFree(q);
   }
 };
+
+// The index arrays a matrix owns: its own, and for a wide matrix its 64-bit
+// pointers and its segments' (whose idx are views, not owned).
+void index_arrays_of(const Matrix &m, std::vector<void *> &out) {
+  for (void *q : {(void *)m.ptr, (void *)m.vptr, (void *)m.blocks, (void *)m.longs,
+                  (void *)m.tp_bounds, (void *)m.ptr64, (void *)m.vptr64})
+    out.push_back(q);
+  if (!m.borrowed_entries) out.push_back(m.idx);
+  for (const Matrix &g : m.segs) index_arrays_of(g, out);
+}
+
+// The per-matrix arrays (values, share partials, failure flag), which are
+// never shared; a segment's values are a view.
+void free_own_arrays(Matrix &m) {
+  for (void *p : {m.partials, (void *)m.err})
+    if (p) cudaFree(p);
+  if (m.vals && !m.borrowed_entries) cudaFree(m.vals);
+  for (Matrix &g : m.segs) free_own_arrays(g);
+}
 }  // namespace
 
 vs_status share_index_arrays(Matrix &m) {
   if (m.index_owner) return VS_OK;
-  IndexArrays *ia = new (std::nothrow)
-      IndexArrays{{(void *)m.ptr, (void *)m.idx, (void *)m.vptr, (void *)m.blocks, (void *)m.longs,
-                   (void *)m.tp_bounds}};
+  IndexArrays *ia = new (std::nothrow) IndexArrays();
   if (!ia) {
     set_error("host allocation failed");
     return VS_ERR_ALLOC;
   }
+  index_arrays_of(m, ia->p);
   m.index_owner = std::shared_ptr<void>(ia, [](void *q) { delete static_cast<IndexArrays *>(q); });
   return VS_OK;
 }
@@ -83,18 +110,20 @@ vs_status share_index_arrays(Matrix &m) {
 void free_matrix(Matrix &m) {
   if (m.index_owner) {
     m.index_owner.reset();  // the index arrays go with their last user
-    for (void *p : {m.vals, m.partials, (void *)m.err})
-      if (p) cudaFree(p);
   } else {
-    for (void *p : {(void *)m.ptr, (void *)m.idx, m.vals, (void *)m.vptr, (void *)m.blocks,
-                    (void *)m.longs, m.partials, (void *)m.tp_bounds, (void *)m.err})
+    std::vector<void *> ix;
+    index_arrays_of(m, ix);
+    for (void *p : ix)
       if (p) cudaFree(p);
   }
+  free_own_arrays(m);
   m.ptr = m.idx = m.vptr = m.tp_bounds = nullptr;
   m.vals = m.partials = nullptr;
   m.blocks = nullptr;
   m.longs = nullptr;
   m.err = nullptr;
+  m.ptr64 = m.vptr64 = nullptr;
+  m.segs.clear();
 }
 
 namespace {
@@ -133,6 +162,13 @@ vs_status kernel_occupancy(const void *kernel, int threads, int smem, int *per_s
   return VS_OK;
 }
 
+// Group size of a matrix's gathers (and of its segments'): forced (g > 0) or
+// the whole matrix's rule (g = 0).
+void set_group_size(Matrix &m, int g) {
+  m.g = g ? g : group_size_rule(m.nnz, m.n_major);
+  for (Matrix &seg : m.segs) seg.g = m.g;
+}
+
 vs_status Scratch::reserve(size_t need, cudaStream_t s) {
   if (need <= bytes) return VS_OK;
   if (p) cudaFreeAsync(p, s);
@@ -159,6 +195,20 @@ using namespace vs;
 
 namespace {
 
+// The failure flags of every matrix a handle's kernels run over: its layout
+// and the attached transpose, or their segments when wide.
+void failure_flags(const vs_handle_s &h, std::vector<int *> &out) {
+  for (const Matrix *m : {&h.A, (const Matrix *)h.T}) {
+    if (!m) continue;
+    if (m->wide) {
+      for (const Matrix &g : m->segs)
+        if (g.err) out.push_back(g.err);
+    } else if (m->err) {
+      out.push_back(m->err);
+    }
+  }
+}
+
 vs_status invalid(const char *msg) {
   set_error(msg);
   return VS_ERR_INVALID;
@@ -168,12 +218,21 @@ bool valid_handle(vs_handle h) { return h != nullptr; }
 
 vs_status build_common(vs_layout layout, int64_t n_rows, int64_t n_cols, int64_t nnz,
                        const int32_t *d_row, const int32_t *d_col, const void *d_val,
-                       vs_dtype dtype, vs_major major, cudaStream_t stream, vs_handle *out) {
+                       vs_dtype dtype, vs_major major, const vs_build_options *opts,
+                       cudaStream_t stream, vs_handle *out) {
   if (!out) return invalid("out handle pointer is NULL");
   *out = nullptr;
   if (n_rows < 0 || n_cols < 0 || nnz < 0) return invalid("negative size");
-  if (n_rows >= (int64_t(1) << 31) || n_cols >= (int64_t(1) << 31) || nnz >= (int64_t(1) << 31)) {
-    set_error("sizes must be below 2^31 (int32 indices)");
+  if (n_rows >= (int64_t(1) << 31) || n_cols >= (int64_t(1) << 31)) {
+    set_error("rows and columns must be below 2^31 (int32 indices)");
+    return VS_ERR_UNSUPPORTED;
+  }
+  const int bits = opts ? opts->pointer_bits : 0;
+  if (bits != 0 && bits != 32 && bits != 64) return invalid("pointer_bits must be 0, 32 or 64");
+  if (opts && opts->segment_entries < 0) return invalid("negative segment_entries");
+  const bool wide = bits == 64 || (bits == 0 && nnz >= (int64_t(1) << 31));
+  if (!wide && nnz >= (int64_t(1) << 31)) {
+    set_error("2^31 or more entries need 64-bit slice pointers (pointer_bits 64 or 0)");
     return VS_ERR_UNSUPPORTED;
   }
   if (dtype != VS_F32 && dtype != VS_F64) return invalid("unknown dtype");
@@ -185,8 +244,10 @@ vs_status build_common(vs_layout layout, int64_t n_rows, int64_t n_cols, int64_t
     return VS_ERR_ALLOC;
   }
   cudaGetDevice(&h->device);
-  vs_status st = build_matrix(h->A, layout, major, dtype, n_rows, n_cols, nnz, d_row, d_col, d_val,
-                              stream);
+  vs_status st = wide ? build_wide(h->A, layout, major, dtype, n_rows, n_cols, nnz, d_row, d_col,
+                                   d_val, opts ? opts->segment_entries : 0, stream)
+                      : build_matrix(h->A, layout, major, dtype, n_rows, n_cols, nnz, d_row, d_col,
+                                     d_val, stream);
   if (st == VS_OK) st = prepare_matrix(h->A, stream);
   if (st != VS_OK) {
     std::string msg = last_error();
@@ -408,14 +469,29 @@ vs_status vs_build_csr(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_
                        const int32_t *d_col, const void *d_val, vs_dtype dtype, vs_major major,
                        cudaStream_t stream, vs_handle *out) {
   return build_common(VS_LAYOUT_CSR, n_rows, n_cols, nnz, d_row, d_col, d_val, dtype, major,
-                      stream, out);
+                      nullptr, stream, out);
 }
 
 vs_status vs_build_vcs(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
                        const int32_t *d_col, const float *d_val, vs_major major,
                        cudaStream_t stream, vs_handle *out) {
   return build_common(VS_LAYOUT_VCS, n_rows, n_cols, nnz, d_row, d_col, d_val, VS_F32, major,
+                      nullptr, stream, out);
+}
+
+vs_status vs_build_csr_opts(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
+                            const int32_t *d_col, const void *d_val, vs_dtype dtype,
+                            vs_major major, const vs_build_options *opts, cudaStream_t stream,
+                            vs_handle *out) {
+  return build_common(VS_LAYOUT_CSR, n_rows, n_cols, nnz, d_row, d_col, d_val, dtype, major, opts,
                       stream, out);
+}
+
+vs_status vs_build_vcs_opts(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
+                            const int32_t *d_col, const float *d_val, vs_major major,
+                            const vs_build_options *opts, cudaStream_t stream, vs_handle *out) {
+  return build_common(VS_LAYOUT_VCS, n_rows, n_cols, nnz, d_row, d_col, d_val, VS_F32, major,
+                      opts, stream, out);
 }
 
 vs_status vs_spmm(vs_handle A, const vs_dense *B, const vs_dense *out, vs_direction dir,
@@ -473,6 +549,8 @@ vs_status vs_spmm_view(vs_handle A, const vs_dense *B, const vs_dense *out, vs_d
         VS_LAUNCH_CHECK();
       }
       mm.vals = dst.p;
+      for (Matrix &g : mm.segs)  // a wide matrix's segments view the mapped values
+        g.vals = static_cast<char *>(dst.p) + (size_t)(vcs ? g.seg_run0 : g.seg_entry0) * es;
       return VS_OK;
     };
     VS_TRY(map_into(m, A->view_vals));
@@ -599,21 +677,26 @@ vs_status vs_spmm_host(vs_handle A, const vs_dense *B_host, const vs_dense *out_
     VS_CUDA(cudaMemcpy2DAsync(Y.p, Y.ld * es, A->stage_out.p, wpad * es, w * es, Y.rows,
                               cudaMemcpyDeviceToHost, stream));
   // the failure flags come back with the output, so one synchronisation ends the call
-  if (!A->host_flags) {
+  std::vector<int *> flags;
+  failure_flags(*A, flags);
+  if ((int)flags.size() > A->host_flag_cap) {
+    if (A->host_flags) cudaFreeHost(A->host_flags);
+    A->host_flags = nullptr;
+    A->host_flag_cap = 0;
     void *hf = nullptr;
-    VS_CUDA(cudaHostAlloc(&hf, 2 * sizeof(int), cudaHostAllocDefault));
+    VS_CUDA(cudaHostAlloc(&hf, sizeof(int) * flags.size(), cudaHostAllocDefault));
     A->host_flags = static_cast<int *>(hf);
+    A->host_flag_cap = (int)flags.size();
   }
-  const Matrix *ms[2] = {&A->A, A->T};
-  for (int k = 0; k < 2; ++k) {
+  for (size_t k = 0; k < flags.size(); ++k) {
     A->host_flags[k] = 0;
-    if (ms[k] && ms[k]->err)
-      VS_CUDA(cudaMemcpyAsync(A->host_flags + k, ms[k]->err, sizeof(int), cudaMemcpyDeviceToHost,
-                              stream));
+    VS_CUDA(cudaMemcpyAsync(A->host_flags + k, flags[k], sizeof(int), cudaMemcpyDeviceToHost,
+                            stream));
   }
   VS_CUDA(cudaStreamSynchronize(stream));
-  if (A->host_flags[0] | A->host_flags[1])
-    return vs_device_status(A, stream);  // clears the flags; reports the gave-up wait
+  int any = 0;
+  for (size_t k = 0; k < flags.size(); ++k) any |= A->host_flags[k];
+  if (any) return vs_device_status(A, stream);  // clears the flags; reports the gave-up wait
   return VS_OK;
 }
 
@@ -635,7 +718,7 @@ vs_status vs_attach_transpose(vs_handle A, cudaStream_t stream) {
     set_error(msg);
     return st;
   }
-  if (A->forced_g) t->g = A->forced_g;
+  if (A->forced_g) set_group_size(*t, A->forced_g);
   A->T = t;
   return VS_OK;
 }
@@ -646,7 +729,7 @@ vs_status vs_force_group_size(vs_handle A, int32_t g) {
     return invalid("group size must be 0, 1, 2, 4, 8, 16 or 32");
   A->forced_g = g;
   for (Matrix *m : {&A->A, A->T})
-    if (m) m->g = g ? g : group_size_rule(m->nnz, m->n_major);
+    if (m) set_group_size(*m, g);
   return VS_OK;
 }
 
@@ -703,6 +786,11 @@ vs_status vs_scale_entries(vs_handle A, const void *factors, cudaStream_t stream
   m.vals = nullptr;
   m.partials = nullptr;
   m.err = nullptr;
+  for (Matrix &g : m.segs) {  // a wide matrix's segments get their own values view and scratch
+    g.vals = nullptr;
+    g.partials = nullptr;
+    g.err = nullptr;
+  }
   auto fail = [&](vs_status st) {
     std::string msg = last_error();
     cudaStreamSynchronize(stream);
@@ -712,12 +800,22 @@ vs_status vs_scale_entries(vs_handle A, const void *factors, cudaStream_t stream
     return st;
   };
   vs_status st = dev_alloc(&m.vals, m.dsize() * (size_t)(m.nnz + 16));
-  if (st == VS_OK && m.n_shares > 0)
-    st = dev_alloc(&m.partials, sizeof(double) * kMaxBlockWidth * (size_t)m.n_shares);
-  if (st == VS_OK) st = dev_alloc((void **)&m.err, sizeof(int));
   if (st != VS_OK) return fail(st);
-  if (cudaMemsetAsync(m.err, 0, sizeof(int), stream) != cudaSuccess)
-    return fail(cuda_status(cudaGetLastError(), "cudaMemsetAsync"));
+  auto scratch = [&](Matrix &g) -> vs_status {
+    if (g.n_shares > 0)
+      VS_TRY(dev_alloc(&g.partials, sizeof(double) * kMaxBlockWidth * (size_t)g.n_shares));
+    VS_TRY(dev_alloc((void **)&g.err, sizeof(int)));
+    VS_CUDA(cudaMemsetAsync(g.err, 0, sizeof(int), stream));
+    return VS_OK;
+  };
+  if (m.wide) {
+    for (Matrix &g : m.segs) {
+      g.vals = static_cast<char *>(m.vals) + (size_t)g.seg_entry0 * m.dsize();
+      if ((st = scratch(g)) != VS_OK) return fail(st);
+    }
+  } else if ((st = scratch(m)) != VS_OK) {
+    return fail(st);
+  }
   if (m.nnz > 0) {
     const unsigned grid = (unsigned)std::min<int64_t>(4096, (m.nnz + 255) / 256);
     if (m.dtype == VS_F64)
@@ -783,11 +881,12 @@ vs_status vs_device_status(vs_handle A, cudaStream_t stream) {
   if (!valid_handle(A)) return invalid("NULL handle");
   VS_CUDA(cudaStreamSynchronize(stream));
   int flags = 0;
-  for (Matrix *m : {&A->A, A->T}) {
-    if (!m || !m->err) continue;
+  std::vector<int *> errs;
+  failure_flags(*A, errs);
+  for (int *e : errs) {
     int f = 0;
-    VS_CUDA(cudaMemcpy(&f, m->err, sizeof f, cudaMemcpyDeviceToHost));
-    if (f) VS_CUDA(cudaMemset(m->err, 0, sizeof f));
+    VS_CUDA(cudaMemcpy(&f, e, sizeof f, cudaMemcpyDeviceToHost));
+    if (f) VS_CUDA(cudaMemset(e, 0, sizeof f));
     flags |= f;
   }
   if (flags) {
@@ -816,19 +915,24 @@ vs_status vs_info(vs_handle A, vs_info_t *info) {
   info->n_chunks = m.n_chunks;
   info->n_blocks = m.n_blocks;
   info->has_transpose = A->T != nullptr;
+  info->pointer_bits = m.wide ? 64 : 32;
+  info->n_segments = m.wide ? (int32_t)m.segs.size() : 1;
   return VS_OK;
 }
 
 vs_status vs_export(vs_handle A, vs_arrays *arrays) {
   if (!valid_handle(A) || !arrays) return invalid("NULL argument");
   const Matrix &m = A->A;
-  arrays->ptr = m.ptr;
+  std::memset(arrays, 0, sizeof *arrays);
+  arrays->ptr = m.wide ? (const void *)m.ptr64 : (const void *)m.ptr;
   arrays->indices = m.idx;
   arrays->values = m.vals;
-  arrays->value_ptr = m.layout == VS_LAYOUT_VCS ? m.vptr : nullptr;
+  if (m.layout == VS_LAYOUT_VCS)
+    arrays->value_ptr = m.wide ? (const void *)m.vptr64 : (const void *)m.vptr;
   arrays->n_major = m.n_major;
   arrays->nnz = m.nnz;
   arrays->n_runs = m.R;
+  arrays->pointer_bits = m.wide ? 64 : 32;
   return VS_OK;
 }
 
@@ -836,7 +940,7 @@ vs_status vs_handle_bytes(vs_handle A, int64_t *layout_bytes, int64_t *scratch_b
   if (!valid_handle(A)) return invalid("NULL handle");
   if (layout_bytes) *layout_bytes = A->A.layout_bytes();
   if (scratch_bytes) {
-    int64_t s = A->A.meta_bytes() + (int64_t)A->tp_partials.bytes +
+    int64_t s = A->A.meta_bytes() + (int64_t)A->tp_partials.bytes + (int64_t)A->wide_tmp.bytes +
                 (int64_t)A->stage_B.bytes + (int64_t)A->stage_out.bytes;
     if (A->T) s += A->T->layout_bytes() + A->T->meta_bytes();
     *scratch_bytes = s;
@@ -856,6 +960,7 @@ vs_status vs_destroy(vs_handle A) {
   if (A->host_flags) cudaFreeHost(A->host_flags);
   A->stage_B.release();
   A->stage_out.release();
+  A->wide_tmp.release();
   A->view_vals.release();
   A->view_tvals.release();
   A->view_X.release();

@@ -7,6 +7,7 @@
 
 #include <memory>
 #include <string>
+#include <vector>
 
 #include "../../include/vs.h"
 
@@ -95,10 +96,35 @@ struct Matrix {
   int tp_chunks = 0;                // C
   int32_t *tp_bounds = nullptr;     // [C+1] block boundaries of the groups
 
-  // When set, the index arrays (ptr, idx, vptr, blocks, longs, tp_bounds) are
-  // shared with other matrices (vs_scale_entries) and freed with the last
-  // reference; vals, partials and err always belong to this matrix.
+  // When set, the index arrays (ptr, idx, vptr, blocks, longs, tp_bounds, and
+  // for a wide matrix ptr64, vptr64 and its segments' index arrays) are shared
+  // with other matrices (vs_scale_entries) and freed with the last reference;
+  // vals, partials and err always belong to this matrix (its segments').
   std::shared_ptr<void> index_owner;
+
+  // Wide matrices: 64-bit slice pointers with int32 indices ("Regridder",
+  // "Why not cuSPARSE").  The stored layout is ptr64 (CSR entry starts, or VCS
+  // run starts) and for VCS vptr64 (run entry starts), with idx and vals as
+  // usual; ptr and vptr stay null.  The kernels run over `segs`: consecutive
+  // slice ranges of fewer than 2^31 entries (and runs), each an ordinary
+  // int32 matrix with slice pointers relative to its first entry (and run)
+  // whose idx and vals view this matrix's arrays.  Every slice keeps the
+  // summation tree it would have in one piece (the group size is the whole
+  // matrix's), so the products have the same bits as an int32 build.
+  bool wide = false;
+  int64_t *ptr64 = nullptr;     // [n_major + 1]
+  int64_t *vptr64 = nullptr;    // VCS: [R + 1]
+  int64_t seg_entries = 0;      // wide: at most this many entries per segment (one longer slice alone)
+  std::vector<Matrix> segs;     // wide: the kernel segments, in slice order
+  // A segment: its first slice in the wide matrix, and where its views of
+  // the wide matrix's arrays start (idx at seg_entry0, VCS values at
+  // seg_run0): the 16-byte boundary at or before its first entry (run), so
+  // its pointers count seg_lead_e entries (seg_lead_r runs) of the previous
+  // segment first, which none of its slices names.  Its idx and vals are
+  // never freed here.
+  int64_t seg_slice0 = 0, seg_entry0 = 0, seg_run0 = 0;
+  int seg_lead_e = 0, seg_lead_r = 0;
+  bool borrowed_entries = false;
 
   size_t dsize() const { return dtype == VS_F64 ? 8 : 4; }
   int64_t layout_bytes() const;
@@ -126,6 +152,7 @@ inline int group_size_rule(int64_t nnz, int64_t n_major) {
 }
 
 void free_matrix(Matrix &m);
+void set_group_size(Matrix &m, int g);
 vs_status dev_alloc(void **p, size_t bytes);
 vs_status share_index_arrays(Matrix &m);
 
@@ -137,7 +164,9 @@ struct vs_handle_s {
   int device = 0;
   vs::Scratch tp_partials;   // two-phase chunk partials
   vs::Scratch stage_B, stage_out;  // host-operand staging (vs_spmm_host)
-  int *host_flags = nullptr;       // pinned: the failure flags of A and T, read back by vs_spmm_host
+  int *host_flags = nullptr;       // pinned: the failure flags of A and T (their segments), read back by vs_spmm_host
+  int host_flag_cap = 0;           // ints host_flags holds
+  vs::Scratch wide_tmp;            // two-phase over a wide matrix: one segment's sum before it is added
   vs::Scratch view_vals, view_tvals, view_X;  // normalized views: mapped values, scaled X
   vs::Scratch floor_sink;                      // vs_gather_floor's per-thread sums
   int forced_g = 0;                            // vs_force_group_size (0: the matrix rule)
@@ -154,8 +183,23 @@ vs_status build_matrix(Matrix &m, vs_layout layout, vs_major major, vs_dtype dty
                        int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *d_row,
                        const int32_t *d_col, const void *d_val, cudaStream_t s);
 
-// Builds the other-major layout of `src` into `dst` from src's own arrays.
+// Builds a wide matrix (64-bit slice pointers, kernel segments of at most
+// `seg_entries` entries) from device COO of any length: the global checks and
+// per-slice counts run over all entries, then each segment's entries are
+// selected in input order and assembled like build_matrix; finally each
+// segment is prepared (prepare_matrix) with the whole matrix's group size.
+// Synchronises `s`.
+vs_status build_wide(Matrix &m, vs_layout layout, vs_major major, vs_dtype dtype, int64_t n_rows,
+                     int64_t n_cols, int64_t nnz, const int32_t *d_row, const int32_t *d_col,
+                     const void *d_val, int64_t seg_entries, cudaStream_t s);
+
+// Builds the other-major layout of `src` into `dst` from src's own arrays
+// (wide when src is; dst then still needs prepare_matrix unless wide).
 vs_status build_transpose(const Matrix &src, Matrix &dst, cudaStream_t s);
+
+// The default segment size of wide matrices: the most entries an int32
+// segment takes with room for the padded over-reads of its arrays.
+constexpr int64_t kMaxSegmentEntries = (int64_t(1) << 31) - (int64_t(1) << 21);
 
 // Fills the matrix-only kernel parameters of `m` (g, chunk tasks, two-phase
 // chunk bounds) from its device arrays.  Synchronises `s`.
