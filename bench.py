@@ -811,7 +811,11 @@ def gpu_arm(args):
               # what ncu measured on the L1/shared data path of the same kernel (the
               # nominal peak above counts 128 useful bytes per clock; random 64-byte
               # rows cannot fill it), null once the kernels changed since the capture
-              "ncu_l1_shared_throughput_pct": recorded_profile("l1pct:" + dom)}
+              "ncu_l1_shared_throughput_pct": recorded_profile("l1pct:" + dom),
+              # shared-memory wavefronts and warp instructions per stored entry of
+              # the same kernel (ncu), under the same digest rule
+              "ncu_shared_wavefronts_per_entry": recorded_profile("wavefronts_per_entry:" + dom),
+              "ncu_instructions_per_entry": recorded_profile("instructions_per_entry:" + dom)}
 
     # ---- CPU baseline: the float64 oracle on host cores (rank 0, N=1 only)
     cpu = None
@@ -863,6 +867,52 @@ def gpu_arm(args):
     return 0
 
 
+def profile_case(args):
+    """One product of one workload, run --warmup + --steps times: the command
+    the ncu captures under profiles/ run (no JSON metric line; a short summary
+    on stdout).  --profile-rows draws a smaller matrix of the workload's recipe,
+    so that a capture of a large configuration stays a few GB."""
+    import torch
+
+    from sparse_dense_products_gb300 import build as vs_build
+    vs_build.build()
+    import sparse_dense_products_gb300 as vs
+    from sparse_dense_products_gb300 import workloads as W
+
+    spec = {name: (layout, major, direction) for name, layout, major, direction in PRODUCTS}
+    layout, major, direction = spec[args.profile_product]
+    dev = torch.device("cuda", 0)
+    coo = W.make(args.profile_workload, seed=0, device=dev, rows=args.profile_rows)
+    fn = vs.build_vcs if layout == "vcs" else vs.build_csr
+    A = fn(coo.rows, coo.cols, coo.vals, (coo.n_rows, coo.n_cols), major)
+    A.attach_transpose()
+    w = args.profile_width
+    B = W.dense(coo.n_cols, w, seed=1, device=dev) if direction == "A@B" else \
+        W.dense(coo.n_rows, w, seed=2, device=dev).t()
+    out = vs.empty_out(A, w, direction)
+    del coo
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        vs.spmm(A, B, direction, out=out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        vs.spmm(A, B, direction, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    info = A.info()
+    lb, _ = A.nbytes()
+    n_x = info["n_cols"] if direction == "A@B" else info["n_rows"]
+    n_y = info["n_rows"] if direction == "A@B" else info["n_cols"]
+    print(json.dumps({"profile": args.profile_product, "workload": args.profile_workload,
+                      "rows": info["n_rows"], "nnz": info["nnz"], "width": w,
+                      "algorithmic_bytes": int(lb + (n_x + n_y) * w * 4),
+                      "ms_per_product_warm": round(e0.elapsed_time(e1) / max(args.steps, 1), 5)}))
+    A.destroy()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -874,7 +924,14 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true", help="omit the cpu_baseline leg")
     ap.add_argument("--skip-extra", action="store_true",
                     help="omit the regridding-shaped, large and skewed workloads")
+    ap.add_argument("--profile-product", choices=[p[0] for p in PRODUCTS],
+                    help="run only this product (for ncu captures), no metric line")
+    ap.add_argument("--profile-workload", default=WORKLOAD)
+    ap.add_argument("--profile-rows", type=int, default=None)
+    ap.add_argument("--profile-width", type=int, default=WIDTH)
     args = ap.parse_args()
+    if args.profile_product:
+        return profile_case(args)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

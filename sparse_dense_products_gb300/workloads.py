@@ -180,11 +180,16 @@ def _zipf_cdf(n_cols: int, s: float, device) -> torch.Tensor:
     return torch.cumsum(k.pow(-s), 0)
 
 
-def make(name: str, seed: int = 0, device="cpu", dtype=torch.float32) -> Coo:
-    """COO triples of a named workload (see the module docstring)."""
+def make(name: str, seed: int = 0, device="cpu", dtype=torch.float32,
+         rows: int | None = None) -> Coo:
+    """COO triples of a named workload (see the module docstring).  ``rows``
+    draws a smaller (or larger) matrix of the same recipe: the same columns and
+    per-row distributions, that many rows."""
     if name not in CONFIGS:
         raise KeyError(f"unknown workload {name!r}; known: {sorted(CONFIGS)}")
     n_rows, n_cols, _ = CONFIGS[name]
+    if rows is not None:
+        n_rows = int(rows)
     g = _gen(seed, device)
     if name == "tiny":
         need = _negbin(n_rows, 10.0, 2, g, device).clamp_(0, n_cols)
