@@ -168,19 +168,20 @@ __device__ __forceinline__ void gather_range(const Staged<TV, VCS> &sv, const XS
 
 // Launch shape.  XS = true keeps X in shared memory: 16 consumer warps, 8
 // stage buffers, one CTA per SM, the slab taking the rest of the SM's shared
-// memory.  XS = false gathers X through L1: CSR runs 2 CTAs per SM of 12
-// consumer warps and 6 stage buffers, each with one producer warp; VCS runs
-// one CTA per SM of 20 consumer warps and 8 stage buffers.  Expanding VCS run
-// values is a chain of shared-memory round trips that one warp per SM cannot
-// keep ahead of the consumers, so VCS splits the producer into one issuing
-// warp and kExpanders expanding warps.
+// memory.  XS = false gathers X through L1, two CTAs per SM so that more
+// operand rows are in flight from L2: CSR with 12 consumer warps and 6 stage
+// buffers each, with one producer warp; VCS with 10 consumer warps and 6 stage
+// buffers each.  Expanding VCS run values is a chain of shared-memory round
+// trips that one warp cannot keep ahead of the consumers, so VCS splits the
+// producer into one issuing warp and kExpanders expanding warps (4 beside the
+// slab's 16 consumers, 2 beside the L1 shape's 10).
 template <bool XS, bool VCS>
 struct GatherShape {
-  static constexpr int kWarps = XS ? 16 : (VCS ? 20 : 12);
-  static constexpr int kStageBufs = XS || VCS ? 8 : 6;
-  static constexpr int kExpanders = VCS ? 4 : 0;
+  static constexpr int kWarps = XS ? 16 : (VCS ? 10 : 12);
+  static constexpr int kStageBufs = XS ? 8 : 6;
+  static constexpr int kExpanders = VCS ? (XS ? 4 : 2) : 0;
   static constexpr int kThreads = (kWarps + 1 + kExpanders) * 32;
-  static constexpr int kMinCtas = XS || VCS ? 1 : 2;
+  static constexpr int kMinCtas = XS ? 1 : 2;
   // Consumer groups: block i of a CTA goes to group i mod kGroups only, so a
   // warp pays the per-block bookkeeping for 1 / kGroups of the blocks.  Each
   // stage buffer always serves the same group (kGroups divides the stages).

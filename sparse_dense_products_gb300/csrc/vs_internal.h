@@ -57,7 +57,7 @@ int64_t launch_count();
 constexpr int kBlockEntries = 1024;
 constexpr int kBlockRuns = 256;
 constexpr int kBlockSlices = 256;
-constexpr int kShareEntries = 512;
+constexpr int kShareEntries = 256;
 constexpr int kWarpsPerCta = 8;   // consumer warps; one more warp produces
 
 // Widest column block one kernel launch handles; wider products loop.
