@@ -778,11 +778,12 @@ vs_status build_wide(Matrix &m, vs_layout layout, vs_major major, vs_dtype dtype
     VS_CUDA(cudaStreamSynchronize(s));
     cudaFree(g.idx);
     g.idx = m.idx + g.seg_entry0;
+    g.borrowed_idx = true;
     if (!vcs) {
       cudaFree(g.vals);
       g.vals = static_cast<char *>(m.vals) + (size_t)g.seg_entry0 * dsize;
+      g.borrowed_vals = true;
     }
-    g.borrowed_entries = true;
     r_base += R_seg;
   }
   m.R = vcs ? r_base : nnz;
@@ -806,6 +807,7 @@ vs_status build_wide(Matrix &m, vs_layout layout, vs_major major, vs_dtype dtype
     for (Matrix &g : m.segs) {
       cudaFree(g.vals);
       g.vals = static_cast<float *>(m.vals) + g.seg_run0;
+      g.borrowed_vals = true;
     }
   }
   // kernel parameters of every segment, with the whole matrix's group size

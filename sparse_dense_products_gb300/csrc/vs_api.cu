@@ -81,7 +81,7 @@ void index_arrays_of(const Matrix &m, std::vector<void *> &out) {
   for (void *q : {(void *)m.ptr, (void *)m.vptr, (void *)m.blocks, (void *)m.longs,
                   (void *)m.tp_bounds, (void *)m.ptr64, (void *)m.vptr64})
     out.push_back(q);
-  if (!m.borrowed_entries) out.push_back(m.idx);
+  if (!m.borrowed_idx) out.push_back(m.idx);
   for (const Matrix &g : m.segs) index_arrays_of(g, out);
 }
 
@@ -90,7 +90,7 @@ void index_arrays_of(const Matrix &m, std::vector<void *> &out) {
 void free_own_arrays(Matrix &m) {
   for (void *p : {m.partials, (void *)m.err})
     if (p) cudaFree(p);
-  if (m.vals && !m.borrowed_entries) cudaFree(m.vals);
+  if (m.vals && !m.borrowed_vals) cudaFree(m.vals);
   for (Matrix &g : m.segs) free_own_arrays(g);
 }
 }  // namespace

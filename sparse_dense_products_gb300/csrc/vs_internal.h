@@ -120,11 +120,11 @@ struct Matrix {
   // the wide matrix's arrays start (idx at seg_entry0, VCS values at
   // seg_run0): the 16-byte boundary at or before its first entry (run), so
   // its pointers count seg_lead_e entries (seg_lead_r runs) of the previous
-  // segment first, which none of its slices names.  Its idx and vals are
-  // never freed here.
+  // segment first, which none of its slices names.  Once they are views
+  // (borrowed_idx, borrowed_vals) they are never freed here.
   int64_t seg_slice0 = 0, seg_entry0 = 0, seg_run0 = 0;
   int seg_lead_e = 0, seg_lead_r = 0;
-  bool borrowed_entries = false;
+  bool borrowed_idx = false, borrowed_vals = false;  // idx / vals are such views
 
   size_t dsize() const { return dtype == VS_F64 ? 8 : 4; }
   int64_t layout_bytes() const;

@@ -64,3 +64,34 @@ def test_step_replays_in_a_cuda_graph():
         assert torch.equal(o, e), f"replay after an operand change differs for product {k}"
     for h in H.values():
         h.destroy()
+
+
+def test_wide_matrix_products_replay_in_a_cuda_graph():
+    """A matrix with 64-bit slice pointers runs one gather per segment: the
+    launches of all segments capture and replay like one product's."""
+    coo = W.random_coo(3000, 1200, 150_000, seed=52, values="counts", sort=False)
+    c = coo.to("cuda")
+    A = vs.build_vcs(c.rows, c.cols, c.vals, (coo.n_rows, coo.n_cols), "row", pointer_bits=64,
+                     segment_entries=20_000).attach_transpose()
+    assert A.info()["n_segments"] > 5
+    Xab = W.dense(coo.n_cols, 16, seed=3).cuda()
+    Xba = W.dense(coo.n_rows, 16, seed=4).cuda()
+    outs = [vs.empty_out(A, 16, "A@B"), vs.empty_out(A, 16, "B@A")]
+
+    def step():
+        vs.spmm(A, Xab, "A@B", out=outs[0])
+        vs.spmm(A, Xba.t(), "B@A", out=outs[1])
+
+    step()
+    torch.cuda.synchronize()
+    eager = [o.clone() for o in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    for o, e in zip(outs, eager):
+        assert torch.equal(o, e)
+    A.destroy()

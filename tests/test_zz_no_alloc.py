@@ -114,3 +114,28 @@ def test_noalloc_on_a_fresh_handle_allocates_nothing():
         assert np.all(np.abs(got - want) <= TOL[torch.float32] * D)
     A.destroy()
     R.destroy()
+
+
+def test_noalloc_on_a_matrix_with_64_bit_pointers():
+    """Wide matrices: the gathers (aligned, and misaligned over the transpose)
+    run allocation-free and equal vs_spmm; the two-phase route, which adds the
+    segments through a temporary, answers VS_ERR_UNSUPPORTED."""
+    coo = W.random_coo(2000, 1500, 80_000, seed=23, values="counts", duplicates=True, sort=False)
+    c = coo.to("cuda")
+    A = vs.build_vcs(c.rows, c.cols, c.vals, (coo.n_rows, coo.n_cols), "row", pointer_bits=64,
+                     segment_entries=9_000)
+    assert A.info()["n_segments"] > 5
+    B, Bt = dense_operand(coo, "A@B", 16, torch.float32, seed=7)
+    want, D = oracle_product(coo, oracle_triples(coo, "vcs", "row"), "A@B", Bt)
+    for _ in range(2):
+        got = gpu_out_rows(_noalloc(A, B, vs.empty_out(A, 16, "A@B"), "A@B"), "A@B")
+        assert np.array_equal(got, gpu_out_rows(vs.spmm(A, B, "A@B"), "A@B"))
+        assert np.all(np.abs(got - want) <= TOL[torch.float32] * D)
+    Bl, _ = dense_operand(coo, "B@A", 16, torch.float32, seed=8)
+    with pytest.raises(L.VsError) as e:
+        _noalloc(A, Bl, vs.empty_out(A, 16, "B@A"), "B@A")
+    assert e.value.status == 8
+    A.attach_transpose()
+    got = gpu_out_rows(_noalloc(A, Bl, vs.empty_out(A, 16, "B@A"), "B@A"), "B@A")
+    assert np.array_equal(got, gpu_out_rows(vs.spmm(A, Bl, "B@A"), "B@A"))
+    A.destroy()
