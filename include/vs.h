@@ -124,7 +124,9 @@ typedef struct {
     int32_t pointer_bits;   /* 32 or 64: the width of the stored slice pointers */
     int32_t n_segments;     /* kernel segments (64-bit pointers: consecutive slice ranges of
                                fewer than 2^31 entries each; 1 otherwise) */
-    int32_t reserved;
+    int32_t two_phase_tiles; /* tiles of output rows of the tiled two-phase scheme (the
+                               deterministic misaligned product without a transpose);
+                               0: the block-stream two-phase scheme runs instead */
 } vs_info_t;
 
 typedef struct {
@@ -153,10 +155,19 @@ typedef struct {
  *                    segment (a slice with more is a segment of its own) --
  *                    lets a small matrix run the many-segment path, as one of
  *                    more than 2^31 entries does.
+ *   two_phase_tile_rows
+ *                    0: 2048; otherwise 1 .. 2048 -- the output rows per tile
+ *                    of the tiled two-phase scheme (VS_TWO_PHASE on a matrix
+ *                    whose minor indices ascend inside every run or slice).
+ *                    With 0 its per-(run, tile) entry offsets are kept only
+ *                    while they take at most half the layout's bytes (else
+ *                    the block-stream scheme runs); a value asked for always
+ *                    builds them.  The tile size changes no result bit: it
+ *                    lets a small matrix run the many-tile path.
  */
 typedef struct {
     int32_t pointer_bits;
-    int32_t reserved;
+    int32_t two_phase_tile_rows;
     int64_t segment_entries;
 } vs_build_options;
 

@@ -43,11 +43,11 @@ class Info(ctypes.Structure):
                 ("has_transpose", ctypes.c_int32),
                 ("pointer_bits", ctypes.c_int32),
                 ("n_segments", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("two_phase_tiles", ctypes.c_int32)]
 
 
 class BuildOptions(ctypes.Structure):
-    _fields_ = [("pointer_bits", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    _fields_ = [("pointer_bits", ctypes.c_int32), ("two_phase_tile_rows", ctypes.c_int32),
                 ("segment_entries", ctypes.c_int64)]
 
 

@@ -168,27 +168,29 @@ def _coo_args(rows: torch.Tensor, cols: torch.Tensor, vals: torch.Tensor):
     return rows.contiguous(), cols.contiguous(), vals.contiguous()
 
 
-def _options(pointer_bits, segment_entries):
-    if pointer_bits is None and segment_entries is None:
+def _options(pointer_bits, segment_entries, two_phase_tile_rows):
+    if pointer_bits is None and segment_entries is None and two_phase_tile_rows is None:
         return None
-    return L.BuildOptions(int(pointer_bits or 0), 0, int(segment_entries or 0))
+    return L.BuildOptions(int(pointer_bits or 0), int(two_phase_tile_rows or 0),
+                          int(segment_entries or 0))
 
 
 def build_csr(rows: torch.Tensor, cols: torch.Tensor, vals: torch.Tensor, shape,
               major: str = "row", *, pointer_bits: int | None = None,
-              segment_entries: int | None = None) -> SparseMatrix:
+              segment_entries: int | None = None,
+              two_phase_tile_rows: int | None = None) -> SparseMatrix:
     """``vs_build_csr`` (``vs_build_csr_opts`` with options): CSR (major="row")
     or CSC (major="col") from device COO.
 
     Each slice keeps its entries in COO input order ("Regridder", "How it is built").
-    ``pointer_bits`` (32, 64; default automatic) and ``segment_entries`` are
-    the build options of include/vs.h.
+    ``pointer_bits`` (32, 64; default automatic), ``segment_entries`` and
+    ``two_phase_tile_rows`` are the build options of include/vs.h.
     """
     rows, cols, vals = _coo_args(rows, cols, vals)
     if vals.dtype not in _DTYPES:
         raise TypeError("values must be float32 or float64")
     h = ctypes.c_void_p()
-    opts = _options(pointer_bits, segment_entries)
+    opts = _options(pointer_bits, segment_entries, two_phase_tile_rows)
     args = (int(shape[0]), int(shape[1]), rows.numel(), rows.data_ptr(), cols.data_ptr(),
             vals.data_ptr(), _DTYPES[vals.dtype], _MAJORS[major])
     stream = ctypes.c_void_p(_stream_ptr(rows.device))
@@ -201,14 +203,15 @@ def build_csr(rows: torch.Tensor, cols: torch.Tensor, vals: torch.Tensor, shape,
 
 def build_vcs(rows: torch.Tensor, cols: torch.Tensor, vals: torch.Tensor, shape,
               major: str = "row", *, pointer_bits: int | None = None,
-              segment_entries: int | None = None) -> SparseMatrix:
+              segment_entries: int | None = None,
+              two_phase_tile_rows: int | None = None) -> SparseMatrix:
     """``vs_build_vcs`` (``vs_build_vcs_opts`` with options): VCSR (major="row")
     or VCSC (major="col") from device COO (float32)."""
     rows, cols, vals = _coo_args(rows, cols, vals)
     if vals.dtype != torch.float32:
         raise TypeError("VCS values are float32")
     h = ctypes.c_void_p()
-    opts = _options(pointer_bits, segment_entries)
+    opts = _options(pointer_bits, segment_entries, two_phase_tile_rows)
     args = (int(shape[0]), int(shape[1]), rows.numel(), rows.data_ptr(), cols.data_ptr(),
             vals.data_ptr(), _MAJORS[major])
     stream = ctypes.c_void_p(_stream_ptr(rows.device))

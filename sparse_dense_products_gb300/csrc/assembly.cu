@@ -814,6 +814,7 @@ vs_status build_wide(Matrix &m, vs_layout layout, vs_major major, vs_dtype dtype
   m.g = group_size_rule(m.nnz, m.n_major);
   m.sorted_segments = true;
   for (Matrix &g : m.segs) {
+    g.tt_req_rows = m.tt_req_rows;
     VS_TRY(prepare_matrix(g, s));
     g.g = m.g;
     m.n_sm = g.n_sm;
@@ -1086,6 +1087,8 @@ vs_status prepare_matrix(Matrix &m, cudaStream_t s) {
     VS_CUDA(cudaMemcpyAsync(m.tp_bounds, bounds.data(), sizeof(int32_t) * (C + 1),
                             cudaMemcpyHostToDevice, s));
   }
+  // ---- the tiled two-phase scheme's per-(run, tile) entry offsets
+  VS_TRY(build_tiled_two_phase(m, ptr, vptr, s));
   VS_CUDA(cudaStreamSynchronize(s));
   return VS_OK;
 }

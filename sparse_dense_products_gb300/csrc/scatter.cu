@@ -879,9 +879,41 @@ vs_status launch_scatter_two_phase_static(const Matrix &m, DenseView X, DenseVie
     return VS_ERR_UNSUPPORTED;
   }
   if (m.n_major == 0 || m.nnz == 0) return launch_zero_fill(Y, w, m.dsize(), s);
+  if (m.tt_rows > 0) {
+    // the group partials in the static array, the column pass narrowed to fit
+    const int64_t es = (int64_t)m.dsize();
+    void *scratch = nullptr;
+    int64_t pass = 64 / es;
+    if (m.tt_groups > 1) {
+      VS_TRY(static_scratch_address(&scratch));
+      const int64_t per_col = (int64_t)m.tt_groups * Y.rows * es;
+      pass = std::min<int64_t>(pass, (int64_t)kStaticScratchBytes / std::max<int64_t>(per_col, 1));
+      if (pass < 1) {
+        set_error("vs_spmm_noalloc: the partial sums need " + std::to_string(per_col) +
+                  " bytes per column; the static scratch holds " +
+                  std::to_string(kStaticScratchBytes) + " bytes");
+        return VS_ERR_UNSUPPORTED;
+      }
+    }
+    return launch_tt_two_phase(m, X, Y, w, scratch, pass, s);
+  }
   if (m.layout == VS_LAYOUT_VCS) return two_phase_static_typed<float, true>(m, X, Y, w, s);
   if (m.dtype == VS_F64) return two_phase_static_typed<double, false>(m, X, Y, w, s);
   return two_phase_static_typed<float, false>(m, X, Y, w, s);
+}
+
+vs_status launch_combine(const void *P, int C, int64_t n_t, int w, void *Y, int64_t ldy,
+                         size_t dsize, int n_sm, cudaStream_t s) {
+  const int64_t total = n_t * w;
+  const unsigned blocks = (unsigned)std::min<int64_t>((int64_t)n_sm * 8, (total + 255) / 256);
+  if (dsize == 8)
+    combine_kernel<double><<<std::max(1u, blocks), 256, 0, s>>>(
+        static_cast<const double *>(P), C, n_t * w, n_t, w, static_cast<double *>(Y), ldy);
+  else
+    combine_kernel<float><<<std::max(1u, blocks), 256, 0, s>>>(
+        static_cast<const float *>(P), C, n_t * w, n_t, w, static_cast<float *>(Y), ldy);
+  VS_LAUNCH_CHECK();
+  return VS_OK;
 }
 
 vs_status launch_zero_fill(DenseView Y, int64_t w, size_t dsize, cudaStream_t s) {
@@ -970,6 +1002,16 @@ vs_status launch_scatter_two_phase(vs_handle_s &h, const Matrix &m, DenseView X,
     }
     if (first) return launch_zero_fill(Y, w, es, s);
     return VS_OK;
+  }
+  if (m.tt_rows > 0) {
+    const size_t es = m.dsize();
+    const int64_t pass = 64 / (int64_t)es;
+    void *part = nullptr;
+    if (m.tt_groups > 1) {
+      VS_TRY(h.tp_partials.reserve((size_t)m.tt_groups * Y.rows * pass * es, s));
+      part = h.tp_partials.p;
+    }
+    return launch_tt_two_phase(m, X, Y, w, part, pass, s);
   }
   if (m.layout == VS_LAYOUT_VCS) return two_phase_typed<float, true>(h, m, X, Y, w, s);
   if (m.dtype == VS_F64) return two_phase_typed<double, false>(h, m, X, Y, w, s);

@@ -61,8 +61,15 @@ int64_t Matrix::meta_bytes() const {
     }
     return b;
   }
+  int64_t tt = 0;  // the tiled two-phase arrays
+  if (tt_rows > 0) {
+    tt = (int64_t)(tt_tiles - 1) * (layout == VS_LAYOUT_VCS ? R : n_major) + (3 * tt_groups + 1) +
+         (int64_t)tt_tiles * tt_groups * (kTtOwners + 1) + (layout == VS_LAYOUT_VCS ? R : 0);
+    tt *= (int64_t)sizeof(int32_t);
+  }
   return (int64_t)sizeof(int4) * 3 * n_blocks + (int64_t)sizeof(int4) * n_long + (int64_t)sizeof(int) +
-         (int64_t)sizeof(double) * kMaxBlockWidth * n_shares + (int64_t)sizeof(int32_t) * (tp_chunks + 1);
+         (int64_t)sizeof(double) * kMaxBlockWidth * n_shares + (int64_t)sizeof(int32_t) * (tp_chunks + 1) +
+         tt;
 }
 
 namespace {
@@ -79,7 +86,8 @@ struct IndexArrays {
 // pointers and its segments' (whose idx are views, not owned).
 void index_arrays_of(const Matrix &m, std::vector<void *> &out) {
   for (void *q : {(void *)m.ptr, (void *)m.vptr, (void *)m.blocks, (void *)m.longs,
-                  (void *)m.tp_bounds, (void *)m.ptr64, (void *)m.vptr64})
+                  (void *)m.tp_bounds, (void *)m.ptr64, (void *)m.vptr64, (void *)m.tt_tab,
+                  (void *)m.tt_run_slice, (void *)m.tt_group, (void *)m.tt_own})
     out.push_back(q);
   if (!m.borrowed_idx) out.push_back(m.idx);
   for (const Matrix &g : m.segs) index_arrays_of(g, out);
@@ -123,6 +131,8 @@ void free_matrix(Matrix &m) {
   m.longs = nullptr;
   m.err = nullptr;
   m.ptr64 = m.vptr64 = nullptr;
+  m.tt_tab = m.tt_run_slice = m.tt_group = m.tt_own = nullptr;
+  m.tt_rows = 0;
   m.segs.clear();
 }
 
@@ -230,6 +240,8 @@ vs_status build_common(vs_layout layout, int64_t n_rows, int64_t n_cols, int64_t
   const int bits = opts ? opts->pointer_bits : 0;
   if (bits != 0 && bits != 32 && bits != 64) return invalid("pointer_bits must be 0, 32 or 64");
   if (opts && opts->segment_entries < 0) return invalid("negative segment_entries");
+  if (opts && (opts->two_phase_tile_rows < 0 || opts->two_phase_tile_rows > kTtRows))
+    return invalid("two_phase_tile_rows must lie in 0 .. 2048");
   const bool wide = bits == 64 || (bits == 0 && nnz >= (int64_t(1) << 31));
   if (!wide && nnz >= (int64_t(1) << 31)) {
     set_error("2^31 or more entries need 64-bit slice pointers (pointer_bits 64 or 0)");
@@ -244,6 +256,7 @@ vs_status build_common(vs_layout layout, int64_t n_rows, int64_t n_cols, int64_t
     return VS_ERR_ALLOC;
   }
   cudaGetDevice(&h->device);
+  h->A.tt_req_rows = opts ? opts->two_phase_tile_rows : 0;
   vs_status st = wide ? build_wide(h->A, layout, major, dtype, n_rows, n_cols, nnz, d_row, d_col,
                                    d_val, opts ? opts->segment_entries : 0, stream)
                       : build_matrix(h->A, layout, major, dtype, n_rows, n_cols, nnz, d_row, d_col,
@@ -708,6 +721,7 @@ vs_status vs_attach_transpose(vs_handle A, cudaStream_t stream) {
     set_error("host allocation failed");
     return VS_ERR_ALLOC;
   }
+  t->tt_req_rows = A->A.tt_req_rows;
   vs_status st = build_transpose(A->A, *t, stream);
   if (st == VS_OK) st = prepare_matrix(*t, stream);
   if (st != VS_OK) {
@@ -743,6 +757,7 @@ vs_status vs_transpose(vs_handle A, cudaStream_t stream, vs_handle *out) {
     return VS_ERR_ALLOC;
   }
   h->device = A->device;
+  h->A.tt_req_rows = A->A.tt_req_rows;
   vs_status st = build_transpose(A->A, h->A, stream);
   if (st == VS_OK) {
     // build_transpose stores A along its other axis; read as the same major
@@ -890,7 +905,9 @@ vs_status vs_device_status(vs_handle A, cudaStream_t stream) {
     flags |= f;
   }
   if (flags) {
-    set_error("a product kernel's bounded wait gave up; its output is not valid");
+    set_error((flags & 2) ? "a product kernel met an entry outside its range (inconsistent "
+                            "matrix arrays); its output is not valid"
+                          : "a product kernel's bounded wait gave up; its output is not valid");
     return VS_ERR_TIMEOUT;
   }
   return VS_OK;
@@ -917,6 +934,7 @@ vs_status vs_info(vs_handle A, vs_info_t *info) {
   info->has_transpose = A->T != nullptr;
   info->pointer_bits = m.wide ? 64 : 32;
   info->n_segments = m.wide ? (int32_t)m.segs.size() : 1;
+  info->two_phase_tiles = m.tt_rows > 0 ? m.tt_tiles : 0;
   return VS_OK;
 }
 

@@ -63,6 +63,16 @@ constexpr int kWarpsPerCta = 8;   // consumer warps; one more warp produces
 // Widest column block one kernel launch handles; wider products loop.
 constexpr int kMaxBlockWidth = 64;
 
+// Tiled two-phase: warps per CTA, row owners the build balances (8 per
+// warp), default and largest rows per tile, CTAs resident per multiprocessor
+// (the tile takes most of its shared memory), and the CTA count the group
+// count aims at (one per multiprocessor of a GB300).
+constexpr int kTtWarps = 16;
+constexpr int kTtOwners = kTtWarps * 8;
+constexpr int kTtRows = 2048;
+constexpr int kTtCtasPerSm = 1;
+constexpr int kTtTargetCtas = 152 * kTtCtasPerSm;
+
 // One stored layout of a matrix: CSR/CSC or VCSR/VCSC.
 struct Matrix {
   vs_layout layout = VS_LAYOUT_CSR;
@@ -96,8 +106,25 @@ struct Matrix {
   int tp_chunks = 0;                // C
   int32_t *tp_bounds = nullptr;     // [C+1] block boundaries of the groups
 
-  // When set, the index arrays (ptr, idx, vptr, blocks, longs, tp_bounds, and
-  // for a wide matrix ptr64, vptr64 and its segments' index arrays) are shared
+  // Tiled two-phase: the output rows (the minor axis) in tiles of tt_rows.
+  // With minor indices ascending in every run (slice), the entries of run r
+  // inside tile k form one range, and tt_tab holds where each such range
+  // starts, so that the CTA of a tile visits its own entries only.  The
+  // entries are cut into tt_groups groups by position (fixed by the matrix
+  // and never by the tiling); tt_own balances each (tile, group)'s rows over
+  // the CTA's row owners by the group's entry counts.  tt_rows == 0: not built
+  // (the block-stream scheme above runs instead).
+  int tt_req_rows = 0;              // rows per tile asked for at build (0: kTtRows)
+  int tt_rows = 0;                  // rows per tile
+  int tt_tiles = 0;                 // tiles over the minor axis
+  int tt_groups = 0;                // entry groups
+  int32_t *tt_tab = nullptr;        // [(tiles-1) * pieces]: first entry of run r at minor >= k*tt_rows, row k-1
+  int32_t *tt_run_slice = nullptr;  // VCS: [R] the slice of every run
+  int32_t *tt_group = nullptr;      // [3*groups+1]: entry bounds, first runs, ends of runs
+  int32_t *tt_own = nullptr;        // [tiles * groups * (kTtOwners+1)] first row of each owner
+
+  // When set, the index arrays (ptr, idx, vptr, blocks, longs, tp_bounds, the
+  // tt_ arrays, and for a wide matrix ptr64, vptr64 and its segments' index arrays) are shared
   // with other matrices (vs_scale_entries) and freed with the last reference;
   // vals, partials and err always belong to this matrix (its segments').
   std::shared_ptr<void> index_owner;
@@ -227,6 +254,24 @@ vs_status launch_gather(const Matrix &m, DenseView X, DenseView Y, int64_t w, cu
 // Misaligned scatter with atomic adds into a zero-filled Y.
 vs_status launch_scatter_atomic(const Matrix &m, DenseView X, DenseView Y, int64_t w,
                                 cudaStream_t s);
+
+// Tiled two-phase (m.tt_rows > 0) over column passes of at most 64 bytes and
+// at most `max_pass` columns: each pass writes Y directly (one group) or the
+// group partials into `part` (groups * Y.rows * max_pass elements), which
+// combine_kernel then adds in group order.
+vs_status launch_tt_two_phase(const Matrix &m, DenseView X, DenseView Y, int64_t w, void *part,
+                              int64_t max_pass, cudaStream_t s);
+
+// Y[t, 0:w] = sum over groups k (in order) of P[k][t, 0:w] (P: [C][n_t][w]
+// of `dsize`-byte elements).
+vs_status launch_combine(const void *P, int C, int64_t n_t, int w, void *Y, int64_t ldy,
+                         size_t dsize, int n_sm, cudaStream_t s);
+
+// Builds the tiled two-phase arrays of `m` (nothing when they do not apply or
+// would exceed half the layout's bytes).  `ptr` / `vptr` are host copies of
+// m's slice and run pointers.  Synchronises `s`.
+vs_status build_tiled_two_phase(Matrix &m, const std::vector<int32_t> &ptr,
+                                const std::vector<int32_t> &vptr, cudaStream_t s);
 
 // Misaligned scatter, deterministic two-phase.
 vs_status launch_scatter_two_phase(vs_handle_s &h, const Matrix &m, DenseView X, DenseView Y,
