@@ -885,7 +885,9 @@ def profile_case(args):
     coo = W.make(args.profile_workload, seed=0, device=dev, rows=args.profile_rows)
     fn = vs.build_vcs if layout == "vcs" else vs.build_csr
     A = fn(coo.rows, coo.cols, coo.vals, (coo.n_rows, coo.n_cols), major)
-    A.attach_transpose()
+    variant = args.profile_variant
+    if variant in ("deterministic", "transposed"):
+        A.attach_transpose()
     w = args.profile_width
     B = W.dense(coo.n_cols, w, seed=1, device=dev) if direction == "A@B" else \
         W.dense(coo.n_rows, w, seed=2, device=dev).t()
@@ -893,19 +895,20 @@ def profile_case(args):
     del coo
     torch.cuda.synchronize()
     for _ in range(args.warmup):
-        vs.spmm(A, B, direction, out=out)
+        vs.spmm(A, B, direction, variant, out=out)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
-        vs.spmm(A, B, direction, out=out)
+        vs.spmm(A, B, direction, variant, out=out)
     e1.record()
     torch.cuda.synchronize()
     info = A.info()
     lb, _ = A.nbytes()
     n_x = info["n_cols"] if direction == "A@B" else info["n_rows"]
     n_y = info["n_rows"] if direction == "A@B" else info["n_cols"]
-    print(json.dumps({"profile": args.profile_product, "workload": args.profile_workload,
+    print(json.dumps({"profile": args.profile_product, "variant": variant,
+                      "workload": args.profile_workload,
                       "rows": info["n_rows"], "nnz": info["nnz"], "width": w,
                       "algorithmic_bytes": int(lb + (n_x + n_y) * w * 4),
                       "ms_per_product_warm": round(e0.elapsed_time(e1) / max(args.steps, 1), 5)}))
@@ -929,6 +932,10 @@ def main():
     ap.add_argument("--profile-workload", default=WORKLOAD)
     ap.add_argument("--profile-rows", type=int, default=None)
     ap.add_argument("--profile-width", type=int, default=WIDTH)
+    ap.add_argument("--profile-variant", default="deterministic",
+                    choices=["deterministic", "two_phase", "atomic", "transposed"],
+                    help="with --profile-product: the variant to run (a misaligned product's "
+                         "deterministic variant runs over the attached transpose)")
     args = ap.parse_args()
     if args.profile_product:
         return profile_case(args)
