@@ -444,7 +444,7 @@ def layout_bytes_of(handles, coo):
 
 def extra_workloads(vs, torch, dev, timed, reps: int, log):
     """The regridding-shaped, large and skewed workloads: ms, GB/s and fraction
-    of the measured HBM copy per product, deterministic and atomic variants,
+    of the measured HBM copy per product, deterministic, atomic and two-phase variants,
     and cuSPARSE beside them."""
     from sparse_dense_products_gb300 import workloads as W
 
@@ -460,7 +460,8 @@ def extra_workloads(vs, torch, dev, timed, reps: int, log):
         for w in (1, 4, 32):
             specs = [("CSR@B", "csr", "row", "A@B", "deterministic"),
                      ("B@CSR", "csr", "row", "B@A", "deterministic"),
-                     ("B@CSR", "csr", "row", "B@A", "atomic")]
+                     ("B@CSR", "csr", "row", "B@A", "atomic"),
+                     ("B@CSR", "csr", "row", "B@A", "two_phase")]
             times = time_product_set(vs, torch, coo, hs, specs, w, dtype, reps, timed, lb)
             times["cusparse"] = cusparse_times(torch, coo, hs, w, dtype, reps, timed, times)
             res.setdefault("regrid", {})[f"{tag}/w{w}"] = times
@@ -482,8 +483,10 @@ def extra_workloads(vs, torch, dev, timed, reps: int, log):
         specs = [("VCSR@B", "vcs", "row", "A@B", "deterministic"),
                  ("VCSC@B", "vcs", "col", "A@B", "deterministic"),
                  ("VCSC@B", "vcs", "col", "A@B", "atomic"),
+                 ("VCSC@B", "vcs", "col", "A@B", "two_phase"),
                  ("B@VCSR", "vcs", "row", "B@A", "deterministic"),
                  ("B@VCSR", "vcs", "row", "B@A", "atomic"),
+                 ("B@VCSR", "vcs", "row", "B@A", "two_phase"),
                  ("B@VCSC", "vcs", "col", "B@A", "deterministic")]
         times = time_product_set(vs, torch, coo, hs, specs, w, torch.float32, reps, timed, lb)
         # cuSPARSE on the index-sorted CSR of the same matrix, beside VCSR@B and B@VCSC
@@ -512,7 +515,8 @@ def extra_workloads(vs, torch, dev, timed, reps: int, log):
     lb = layout_bytes_of(hs, coo)
     specs = [("CSR@B", "csr", "row", "A@B", "deterministic"),
              ("B@CSR", "csr", "row", "B@A", "deterministic"),
-             ("B@CSR", "csr", "row", "B@A", "atomic")]
+             ("B@CSR", "csr", "row", "B@A", "atomic"),
+             ("B@CSR", "csr", "row", "B@A", "two_phase")]
     sk = time_product_set(vs, torch, coo, hs, specs, 64, torch.float32, reps, timed, lb)
     sk["cusparse"] = cusparse_times(torch, coo, hs, 64, torch.float32, reps, timed, sk)
     sk["nnz"] = coo.nnz

@@ -160,10 +160,14 @@ typedef struct {
  *                    of the tiled two-phase scheme (VS_TWO_PHASE on a matrix
  *                    whose minor indices ascend inside every run or slice).
  *                    With 0 its per-(run, tile) entry offsets are kept only
- *                    while they take at most half the layout's bytes (else
- *                    the block-stream scheme runs); a value asked for always
- *                    builds them.  The tile size changes no result bit: it
- *                    lets a small matrix run the many-tile path.
+ *                    while they take at most half the layout's bytes; a value
+ *                    asked for always builds them; -1 never does.  Without
+ *                    them VS_TWO_PHASE sorts each call's entries into
+ *                    (tile, group) buckets in handle scratch (at most 1,024
+ *                    buckets; about 10-14 bytes per entry), or, past that,
+ *                    streams the matrix's blocks per tile.  The tile size
+ *                    changes no result bit: it lets a small matrix run the
+ *                    many-tile path.
  */
 typedef struct {
     int32_t pointer_bits;

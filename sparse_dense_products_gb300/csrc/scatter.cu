@@ -1013,6 +1013,7 @@ vs_status launch_scatter_two_phase(vs_handle_s &h, const Matrix &m, DenseView X,
     }
     return launch_tt_two_phase(m, X, Y, w, part, pass, s);
   }
+  if (tb_applies(m, Y.rows)) return launch_tb_two_phase(h, m, X, Y, w, s);
   if (m.layout == VS_LAYOUT_VCS) return two_phase_typed<float, true>(h, m, X, Y, w, s);
   if (m.dtype == VS_F64) return two_phase_typed<double, false>(h, m, X, Y, w, s);
   return two_phase_typed<float, false>(h, m, X, Y, w, s);

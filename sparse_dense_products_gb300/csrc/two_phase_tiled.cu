@@ -545,7 +545,9 @@ vs_status build_tiled_two_phase(Matrix &m, const std::vector<int32_t> &ptr,
   m.tt_rows = m.tt_tiles = m.tt_groups = 0;
   // a wide matrix's segments view its arrays past leading entries no slice
   // names: they keep the block-stream scheme
-  if (m.wide || m.borrowed_idx || m.nnz == 0 || m.n_minor == 0 || m.n_major == 0) return VS_OK;
+  if (m.wide || m.borrowed_idx || m.nnz == 0 || m.n_minor == 0 || m.n_major == 0 ||
+      m.tt_req_rows < 0)
+    return VS_OK;
   const bool vcs = m.layout == VS_LAYOUT_VCS;
   const int64_t pieces = vcs ? m.R : m.n_major;
   const std::vector<int32_t> &st = vcs ? vptr : ptr;  // [pieces + 1] entry starts

@@ -240,8 +240,8 @@ vs_status build_common(vs_layout layout, int64_t n_rows, int64_t n_cols, int64_t
   const int bits = opts ? opts->pointer_bits : 0;
   if (bits != 0 && bits != 32 && bits != 64) return invalid("pointer_bits must be 0, 32 or 64");
   if (opts && opts->segment_entries < 0) return invalid("negative segment_entries");
-  if (opts && (opts->two_phase_tile_rows < 0 || opts->two_phase_tile_rows > kTtRows))
-    return invalid("two_phase_tile_rows must lie in 0 .. 2048");
+  if (opts && (opts->two_phase_tile_rows < -1 || opts->two_phase_tile_rows > kTtRows))
+    return invalid("two_phase_tile_rows must lie in -1 .. 2048");
   const bool wide = bits == 64 || (bits == 0 && nnz >= (int64_t(1) << 31));
   if (!wide && nnz >= (int64_t(1) << 31)) {
     set_error("2^31 or more entries need 64-bit slice pointers (pointer_bits 64 or 0)");
@@ -958,8 +958,8 @@ vs_status vs_handle_bytes(vs_handle A, int64_t *layout_bytes, int64_t *scratch_b
   if (!valid_handle(A)) return invalid("NULL handle");
   if (layout_bytes) *layout_bytes = A->A.layout_bytes();
   if (scratch_bytes) {
-    int64_t s = A->A.meta_bytes() + (int64_t)A->tp_partials.bytes + (int64_t)A->wide_tmp.bytes +
-                (int64_t)A->stage_B.bytes + (int64_t)A->stage_out.bytes;
+    int64_t s = A->A.meta_bytes() + (int64_t)A->tp_partials.bytes + (int64_t)A->tb_scratch.bytes +
+                (int64_t)A->wide_tmp.bytes + (int64_t)A->stage_B.bytes + (int64_t)A->stage_out.bytes;
     if (A->T) s += A->T->layout_bytes() + A->T->meta_bytes();
     *scratch_bytes = s;
   }
@@ -975,6 +975,7 @@ vs_status vs_destroy(vs_handle A) {
     delete A->T;
   }
   A->tp_partials.release();
+  A->tb_scratch.release();
   if (A->host_flags) cudaFreeHost(A->host_flags);
   A->stage_B.release();
   A->stage_out.release();

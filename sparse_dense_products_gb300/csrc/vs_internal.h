@@ -72,6 +72,8 @@ constexpr int kTtOwners = kTtWarps * 8;
 constexpr int kTtRows = 2048;
 constexpr int kTtCtasPerSm = 1;
 constexpr int kTtTargetCtas = 152 * kTtCtasPerSm;
+// Bucketed two-phase: at most this many (tile, group) buckets.
+constexpr int kTbMaxBuckets = 1024;
 
 // One stored layout of a matrix: CSR/CSC or VCSR/VCSC.
 struct Matrix {
@@ -190,6 +192,7 @@ struct vs_handle_s {
   vs::Matrix *T = nullptr;  // exact transpose (other major), once attached
   int device = 0;
   vs::Scratch tp_partials;   // two-phase chunk partials
+  vs::Scratch tb_scratch;    // bucketed two-phase: the call's records and partials
   vs::Scratch stage_B, stage_out;  // host-operand staging (vs_spmm_host)
   int *host_flags = nullptr;       // pinned: the failure flags of A and T (their segments), read back by vs_spmm_host
   int host_flag_cap = 0;           // ints host_flags holds
@@ -266,6 +269,12 @@ vs_status launch_tt_two_phase(const Matrix &m, DenseView X, DenseView Y, int64_t
 // of `dsize`-byte elements).
 vs_status launch_combine(const void *P, int C, int64_t n_t, int w, void *Y, int64_t ldy,
                          size_t dsize, int n_sm, cudaStream_t s);
+
+// Bucketed two-phase: whether it serves `m` (no tiled arrays kept) for an output
+// of n_out rows, and the product (handle scratch holds each call's records).
+bool tb_applies(const Matrix &m, int64_t n_out);
+vs_status launch_tb_two_phase(vs_handle_s &h, const Matrix &m, DenseView X, DenseView Y, int64_t w,
+                              cudaStream_t s);
 
 // Builds the tiled two-phase arrays of `m` (nothing when they do not apply or
 // would exceed half the layout's bytes).  `ptr` / `vptr` are host copies of

@@ -134,7 +134,7 @@ def test_large_count_matrix_four_vcs_directions():
         A.attach_transpose()
         for direction in ("A@B", "B@A"):
             misaligned = (direction == "A@B") != (major == "row")
-            variants = ["deterministic", "atomic"] if misaligned else ["deterministic"]
+            variants = ["deterministic", "atomic", "two_phase"] if misaligned else ["deterministic"]
             for w in (8, 32):
                 _check_product(coo, A, direction, w, variants, sel_rows, sel_cols, seed=10 + w)
         A.destroy()
@@ -155,5 +155,6 @@ def test_skewed_power_law_csr_width_64():
     del arr
     _check_product(coo, A, "A@B", 64, ["deterministic"], sel_rows, sel_cols, seed=7)
     A.attach_transpose()
-    _check_product(coo, A, "B@A", 64, ["deterministic", "atomic"], sel_rows, sel_cols, seed=8)
+    _check_product(coo, A, "B@A", 64, ["deterministic", "atomic", "two_phase"], sel_rows, sel_cols,
+                   seed=8)
     A.destroy()
