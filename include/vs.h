@@ -160,9 +160,8 @@ typedef struct {
  *                    of the tiled two-phase scheme (VS_TWO_PHASE on a matrix
  *                    whose minor indices ascend inside every run or slice).
  *                    With 0 its per-(run, tile) entry offsets are kept only
- *                    while they take at most half the layout's bytes and the
- *                    pieces they mark hold 4 entries or more on average; a
- *                    value asked for always builds them; -1 never does.  Without
+ *                    while they take at most half the layout's bytes; a value
+ *                    asked for always builds them; -1 never does.  Without
  *                    them VS_TWO_PHASE sorts each call's entries into
  *                    (tile, group) buckets in handle scratch (at most 1,024
  *                    buckets; about 10-14 bytes per entry), or, past that,

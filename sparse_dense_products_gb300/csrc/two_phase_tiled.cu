@@ -559,12 +559,7 @@ vs_status build_tiled_two_phase(Matrix &m, const std::vector<int32_t> &ptr,
   const int64_t T = (m.n_minor + TR - 1) / TR;
   if (T > 1 && !m.sorted_segments) return VS_OK;  // a tile's entries of a run are no range
   const int64_t tab_n = (T - 1) * pieces;
-  // by default, only where the pieces are worth their per-piece work (at least
-  // four entries on average) and the offsets take at most half the layout;
-  // else the bucketed scheme serves the product
-  if (m.tt_req_rows == 0 && T > 1 &&
-      (m.nnz < 4 * pieces * T || (int64_t)sizeof(int32_t) * tab_n > m.layout_bytes() / 2))
-    return VS_OK;
+  if (m.tt_req_rows == 0 && (int64_t)sizeof(int32_t) * tab_n > m.layout_bytes() / 2) return VS_OK;
   if (T > (int64_t(1) << 30)) return VS_OK;
 
   // groups: from the default tiling, so that a requested tile size changes no bits

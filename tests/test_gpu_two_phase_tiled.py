@@ -81,7 +81,7 @@ def _coo(seed=81, dtype=torch.float32, values="counts", sort=True):
 @pytest.mark.parametrize("layout,major,direction", MISALIGNED)
 def test_tiled_matches_oracle_and_is_fixed_by_the_matrix(layout, major, direction):
     coo = _coo()
-    A = _build(coo, layout, major, two_phase_tile_rows=TILE)
+    A = _build(coo, layout, major)
     tiles = A.info()["two_phase_tiles"]
     assert tiles == (_n_out(coo, major) + TILE - 1) // TILE == 2, A.info()
     small = _build(coo, layout, major, two_phase_tile_rows=100)
@@ -159,7 +159,7 @@ def test_tiled_skewed_rows_and_tiny_matrices():
     vals = torch.empty(120_000, dtype=torch.float64).geometric_(0.5, generator=g).float()
     coo = W.Coo(n_rows, n_cols, rows[o], cols[o], vals[o])
     for layout in ("vcs", "csr"):
-        A = _build(coo, layout, "row", two_phase_tile_rows=TILE)
+        A = _build(coo, layout, "row")
         assert A.info()["two_phase_tiles"] == 2
         tri = oracle_triples(coo, layout, "row")
         B, Bt = dense_operand(coo, "B@A", 16, torch.float32, seed=3)
@@ -200,31 +200,3 @@ def test_tiled_main_workload_two_phase_vs_oracle_sampled():
         assert torch.equal(vs.spmm(A, B, direction, "two_phase"), out)
         A.destroy()
     del oracle
-
-
-def test_default_build_keeps_offsets_only_for_pieces_worth_them():
-    """By default the per-(run, tile) offsets are kept only where the pieces
-    average 4 entries or more (and the table stays within half the layout):
-    the main workload's VCSC (60,000 output rows, pieces of ~9 entries) keeps
-    them, rows of ~3 entries over 2,290 output columns do not (the bucketed
-    scheme serves them), while long columns over 40,000 output rows keep them."""
-    from gpu_helpers import workload
-    main = workload("main")
-    A = _build(main, "vcs", "col")
-    assert A.info()["two_phase_tiles"] == 30
-    A.destroy()
-    short = W.random_coo(40_000, 2290, 120_000, seed=71, values="counts", duplicates=False)
-    B_ = _build(short, "csr", "row")
-    assert B_.info()["two_phase_tiles"] == 0
-    tri = oracle_triples(short, "csr", "row")
-    X, Xt = dense_operand(short, "B@A", 4, torch.float32, seed=2)
-    want, D = oracle_product(short, tri, "B@A", Xt)
-    out = vs.spmm(B_, X, "B@A", "two_phase")
-    assert_close(gpu_out_rows(out, "B@A"), want, D, TOL[torch.float32], "bucketed, short rows")
-    assert torch.equal(vs.spmm(B_, X, "B@A", "two_phase"), out)
-    B_.destroy()
-    assert _build(short, "csr", "col").info()["two_phase_tiles"] == 0  # pieces of ~2.6 entries
-    tall = W.random_coo(40_000, 100, 120_000, seed=72, values="counts", duplicates=False)
-    C = _build(tall, "csr", "col")  # 20 tiles of 40,000 output rows, pieces of ~60 entries
-    assert C.info()["two_phase_tiles"] == (40_000 + TILE - 1) // TILE
-    C.destroy()
