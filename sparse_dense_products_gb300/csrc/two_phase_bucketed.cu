@@ -69,41 +69,78 @@ __device__ __forceinline__ int group_of(const int32_t *bounds, int C, int b) {
   return lo;
 }
 
+// A warp's shared-memory view of one block's pieces (runs for VCS, slices for
+// CSR): the first entry of each (clipped to the block), then the block's end;
+// the slice of each; the run value of each (VCS).
+constexpr int kTbPieces = (kCapRuns > kCapSlices ? kCapRuns : kCapSlices) + 1;
+struct PieceTab {
+  int *start;  // [kTbPieces]
+  int *slice;  // [kTbPieces]
+  float *val;  // [kTbPieces]
+  static constexpr int kBytes = kTbPieces * 12;
+  __device__ __forceinline__ static PieceTab at(unsigned char *base) {
+    return PieceTab{reinterpret_cast<int *>(base), reinterpret_cast<int *>(base + kTbPieces * 4),
+                    reinterpret_cast<float *>(base + kTbPieces * 8)};
+  }
+};
+
 // Warp-wide: calls f(e, slice, value, valid) for the entries of block k in
 // entry order, 32 at a time (every lane calls f the same number of times).
+// The block's pieces go to `pt` first; a lane finds its entry's piece there.
 template <typename T, bool VCS, class F>
-__device__ __forceinline__ void block_entries(const TbSort &a, const Block &k, F &&f) {
+__device__ __forceinline__ void block_entries(const TbSort &a, const Block &k, const PieceTab &pt,
+                                              F &&f) {
   const int lane = threadIdx.x & 31;
-  auto piece = [&](int sl, int lo, int hi, bool per_run, T rv) {
-    for (int b0 = lo; b0 < hi; b0 += 32) {
-      const int e = b0 + lane;
-      const bool ok = e < hi;
-      const T v = !ok ? T(0) : (per_run ? rv : static_cast<const T *>(a.vals)[e]);
-      f(e, sl, v, ok);
+  int n = 0;  // pieces
+  if (VCS) {
+    n = k.r1 - k.r0;
+    for (int i = lane; i < n; i += 32) {
+      const int r = k.r0 + i;
+      pt.start[i] = max(a.vptr[r], k.e0);
+      pt.val[i] = static_cast<const float *>(a.vals)[r];
+      if (k.type != 0) pt.slice[i] = k.s0;
     }
-  };
-  const int s_lo = k.s0, s_hi = k.type == 0 ? k.s1 : k.s0 + 1;
-  for (int sl = s_lo; sl < s_hi; ++sl) {
-    if (VCS) {
-      const int r_lo = k.type == 0 ? a.ptr[sl] : k.r0;
-      const int r_hi = k.type == 0 ? a.ptr[sl + 1] : k.r1;
-      for (int r = r_lo; r < r_hi; ++r) {
-        const int lo = max(a.vptr[r], k.e0), hi = min(a.vptr[r + 1], k.e1);
-        piece(sl, lo, hi, true, (T) static_cast<const float *>(a.vals)[r]);
-      }
-    } else {
-      const int lo = k.type == 0 ? a.ptr[sl] : k.e0;
-      const int hi = k.type == 0 ? a.ptr[sl + 1] : k.e1;
-      piece(sl, lo, hi, false, T(0));
+    if (k.type == 0)  // the slice of every run: each lane takes slices, writes their runs
+      for (int sl = k.s0 + lane; sl < k.s1; sl += 32)
+        for (int r = a.ptr[sl]; r < a.ptr[sl + 1]; ++r) pt.slice[r - k.r0] = sl;
+  } else if (k.type == 0) {
+    n = k.s1 - k.s0;
+    for (int i = lane; i < n; i += 32) {
+      pt.start[i] = a.ptr[k.s0 + i];
+      pt.slice[i] = k.s0 + i;
+    }
+  } else {
+    n = 1;
+    if (lane == 0) {
+      pt.start[0] = k.e0;
+      pt.slice[0] = k.s0;
     }
   }
+  __syncwarp();
+  for (int b0 = k.e0; b0 < k.e1; b0 += 32) {
+    const int e = b0 + lane;
+    const bool ok = e < k.e1;
+    int lo = 0, hi = n - 1;  // the last piece starting at or before e (empty ones start there too)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (pt.start[mid] <= e)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const T v = !ok ? T(0) : (VCS ? (T)pt.val[lo] : static_cast<const T *>(a.vals)[e]);
+    f(e, pt.slice[lo], v, ok);
+  }
+  __syncwarp();  // the table is rewritten for the warp's next block
 }
 
 // Pass 1: entries per (superblock, bucket).
 template <typename T, bool VCS>
 __global__ void __launch_bounds__(kTbWarps * 32) tb_count_kernel(const TbSort a) {
-  extern __shared__ int hist[];  // [T*C]
+  extern __shared__ __align__(16) unsigned char tb_smem[];
   const int B = a.T * a.C, wid = threadIdx.x >> 5;
+  int *hist = reinterpret_cast<int *>(tb_smem);  // [T*C]
+  const PieceTab pt = PieceTab::at(tb_smem + (B * 4 + 15) / 16 * 16 + wid * PieceTab::kBytes);
   for (int q = threadIdx.x; q < B; q += blockDim.x) hist[q] = 0;
   __syncthreads();
   const int b_lo = blockIdx.x * kTbBlocksPerCta;
@@ -111,7 +148,7 @@ __global__ void __launch_bounds__(kTbWarps * 32) tb_count_kernel(const TbSort a)
   for (int b = b_lo + wid; b < b_hi; b += kTbWarps) {
     const int c = group_of(a.bounds, a.C, b);
     const Block k = load_block(a.blocks, b);
-    block_entries<T, VCS>(a, k, [&](int e, int, T, bool ok) {
+    block_entries<T, VCS>(a, k, pt, [&](int e, int, T, bool ok) {
       if (ok) atomicAdd(&hist[(a.idx[e] / a.tile_rows) * a.C + c], 1);
     });
   }
@@ -149,8 +186,11 @@ __global__ void __launch_bounds__(1024) tb_base_kernel(const int *tot, int B, in
 // entries, lanes in entry order.
 template <typename T, bool VCS>
 __global__ void __launch_bounds__(kTbWarps * 32) tb_place_kernel(const TbSort a) {
-  extern __shared__ int cur[];  // [kTbWarps][T*C]
+  extern __shared__ __align__(16) unsigned char tb_smem[];
   const int B = a.T * a.C, wid = threadIdx.x >> 5;
+  int *cur = reinterpret_cast<int *>(tb_smem);  // [kTbWarps][T*C]
+  const PieceTab pt =
+      PieceTab::at(tb_smem + (kTbWarps * B * 4 + 15) / 16 * 16 + wid * PieceTab::kBytes);
   const unsigned lt = lanemask_lt();
   for (int q = threadIdx.x; q < kTbWarps * B; q += blockDim.x) cur[q] = 0;
   __syncthreads();
@@ -161,7 +201,7 @@ __global__ void __launch_bounds__(kTbWarps * 32) tb_place_kernel(const TbSort a)
   for (int b = b_lo; b < b_hi; ++b) {
     const int c = group_of(a.bounds, a.C, b);
     const Block k = load_block(a.blocks, b);
-    block_entries<T, VCS>(a, k, [&](int e, int, T, bool ok) {
+    block_entries<T, VCS>(a, k, pt, [&](int e, int, T, bool ok) {
       const int bk = ok ? (a.idx[e] / a.tile_rows) * a.C + c : -1;
       const unsigned peers = __match_any_sync(kFullMask, bk);
       if (ok && (peers & lt) == 0) mine[bk] += __popc(peers);
@@ -182,7 +222,7 @@ __global__ void __launch_bounds__(kTbWarps * 32) tb_place_kernel(const TbSort a)
   for (int b = b_lo; b < b_hi; ++b) {
     const int c = group_of(a.bounds, a.C, b);
     const Block k = load_block(a.blocks, b);
-    block_entries<T, VCS>(a, k, [&](int e, int sl, T v, bool ok) {
+    block_entries<T, VCS>(a, k, pt, [&](int e, int sl, T v, bool ok) {
       const int row = ok ? a.idx[e] : 0;
       const int t = row / a.tile_rows;
       const int bk = ok ? t * a.C + c : -1;
@@ -469,14 +509,20 @@ vs_status tb_typed(vs_handle_s &h, const Matrix &m, DenseView X, DenseView Y, in
   so.rec_row = reinterpret_cast<uint16_t *>(sp + o_row);
   void *part = sp + o_part;
   // the records, once per call
-  tb_count_kernel<T, VCS><<<n_sb, kTbWarps * 32, sizeof(int) * B, s>>>(so);
-  VS_LAUNCH_CHECK();
+  {
+    const int smem = (B * 4 + 15) / 16 * 16 + kTbWarps * PieceTab::kBytes;
+    int resident = 0;  // (raises the kernel's shared-memory limit once)
+    VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(tb_count_kernel<T, VCS>),
+                            kTbWarps * 32, smem, &resident));
+    tb_count_kernel<T, VCS><<<n_sb, kTbWarps * 32, smem, s>>>(so);
+    VS_LAUNCH_CHECK();
+  }
   tb_scan_kernel<<<B, 256, 0, s>>>(so.counts, n_sb, B, so.tot);
   VS_LAUNCH_CHECK();
   tb_base_kernel<<<1, 1024, 0, s>>>(so.tot, B, so.base);
   VS_LAUNCH_CHECK();
   {
-    const int smem = (int)(sizeof(int) * kTbWarps * B);
+    const int smem = (kTbWarps * B * 4 + 15) / 16 * 16 + kTbWarps * PieceTab::kBytes;
     int resident = 0;  // (raises the kernel's shared-memory limit once)
     VS_TRY(kernel_occupancy(reinterpret_cast<const void *>(tb_place_kernel<T, VCS>),
                             kTbWarps * 32, smem, &resident));
