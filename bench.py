@@ -551,17 +551,28 @@ def gpu_arm(args):
     coo = W.make(WORKLOAD, seed=0, device=dev)
     n_rows, n_cols = coo.n_rows, coo.n_cols
 
-    # ---- assembly (timed, reported; not part of the step)
+    # ---- assembly (timed, reported; not part of the step).  Each layout is
+    # built twice: the first build of a process also loads the assembly
+    # kernels and grows the allocator's pools, so the second one is reported
+    # (the first beside it).
     assembly = {}
+    assembly_first = {}
     handles = {}
     for key, fn in ((("vcs", "row"), vs.build_vcs), (("vcs", "col"), vs.build_vcs),
                     (("csr", "row"), vs.build_csr)):
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        handles[key] = fn(coo.rows, coo.cols, coo.vals, (n_rows, n_cols), key[1])
-        torch.cuda.synchronize()
-        assembly[f"{'V' if key[0] == 'vcs' else ''}CS{'R' if key[1] == 'row' else 'C'}"] = \
-            round((time.perf_counter() - t0) * 1e3, 3)
+        name = f"{'V' if key[0] == 'vcs' else ''}CS{'R' if key[1] == 'row' else 'C'}"
+        for rep in range(2):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            h = fn(coo.rows, coo.cols, coo.vals, (n_rows, n_cols), key[1])
+            torch.cuda.synchronize()
+            ms = round((time.perf_counter() - t0) * 1e3, 3)
+            if rep == 0:
+                assembly_first[name] = ms
+                h.destroy()
+            else:
+                assembly[name] = ms
+                handles[key] = h
     for h in handles.values():
         h.attach_transpose()
 
@@ -861,6 +872,7 @@ def gpu_arm(args):
         "no_transpose": no_transpose,
         "extra_workloads": extra,
         "assembly_ms": assembly,
+        "assembly_first_build_ms": assembly_first,
         "wall_s_timed_region": round(wall, 3),
     }
     if rank == 0:
